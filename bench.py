@@ -1,0 +1,423 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path for one batch: the new token of every sequence
+is written to its slot and attended together with the cached tokens (fused
+append + balanced split-KV decode + log-sum-exp merge, pa_append_decode).
+Default workload: LLaMA-3-8B layout (32 q / 8 kv heads, d 128, bf16), batch 64,
+lognormal lengths (median 600, sigma 0.8, clipped to [16, 8192]), 16-token
+blocks at random places in a pool 1.25x the needed size.
+
+Output: one JSON line (rank 0).  `value` is algorithmic bytes per step (K/V
+of every attended token, the new rows written, q, output, tables, lengths)
+over the device time of the step, summed over ranks, in GB/s.  Inputs are
+resident in HBM; L2 is flushed (a 2x-L2 buffer is written) before every timed
+step.  `e2e` repeats the measurement through the same public calls with the
+step's inputs copied from pinned host memory and the output copied back
+inside the timed region.
+
+`--impl reference` times the fp64 CPU oracle instead (the only other arm this
+repository has), on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV GB/s vs GB300 HBM peak; µs per decode step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=3, help="config number (default: the batch-64 LLaMA-3-8B layout)")
+    ap.add_argument("--partition-blocks", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(cfg, dec_lens, tables_width, out_bytes=2):
+    """Algorithmic bytes of one fused append + decode step."""
+    B = len(dec_lens)
+    Hq, Hkv, d = cfg.n_q_heads, cfg.n_kv_heads, cfg.d_head
+    kv = int(np.sum(dec_lens)) * Hkv * d * 2 * 2          # K and V of every attended token
+    new_rows = B * Hkv * d * 2 * 2                       # the new K/V rows written to the pool
+    q = B * Hq * d * 2
+    out = B * Hq * d * out_bytes
+    nb = int(np.sum(-(-dec_lens // 16)))
+    table = 4 * nb + 4 * B
+    return {"kv": kv, "new_rows": new_rows, "q": q, "out": out, "tables": table,
+            "total": kv + new_rows + q + out + table}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, enabled=True):
+        self.proc = None
+        self.device_index = device_index
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def traffic_record(workload):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
+    or None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[str(workload)]
+        src = os.path.join(ROOT, "paged_kv_cache_227_gb300", "csrc", "decode.cu")
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("decode_cu_sha256") != digest:
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+def build_inputs(cfg_key, rank, device):
+    import paged_kv_cache_227_gb300 as pa
+    from workloads import CONFIGS, build_tables, make_case
+    cfg = CONFIGS[cfg_key]
+    case = make_case(cfg, seed=1000 + cfg.key + 7919 * rank)
+    alloc = pa.BlockAllocator(case.num_blocks, 16, case.free_order)
+    tables, slots, cows, dec_lens = build_tables(case, alloc)
+    assert not cows, "the benchmark workloads append into fresh or private blocks"
+    return pa, cfg, case, tables, slots, dec_lens
+
+
+def run_ours(args, rank, world, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    pa, cfg, case, tables, slots, dec_lens = build_inputs(args.workload, rank, device)
+    pool = pa.Pool(case.num_blocks, cfg.n_kv_heads, cfg.torch_dtype)
+    pool.k.copy_(case.k_pool.to(device))
+    pool.v.copy_(case.v_pool.to(device))
+    q = case.q.to(device)
+    k_new = case.k_new.to(device)
+    v_new = case.v_new.to(device)
+    bt = torch.from_numpy(tables).to(device)
+    sl = torch.from_numpy(dec_lens).to(device)
+    out = torch.empty(q.shape, dtype=cfg.torch_dtype, device=device)
+    ws = pa.workspace_for(pool, q, bt, args.partition_blocks)
+    nbytes = step_bytes(cfg, dec_lens, tables.shape[1])
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    # the step, with its ctypes arguments marshalled once
+    import ctypes
+    fn = pa.lib.pa_append_decode
+    argv = (pool.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_new.data_ptr()),
+            ctypes.c_void_p(v_new.data_ptr()), ctypes.c_void_p(bt.data_ptr()), bt.shape[1],
+            ctypes.c_void_p(sl.data_ptr()), q.shape[0], q.shape[1], float(case.scale),
+            ctypes.c_void_p(out.data_ptr()), pa._DTYPE_CODE[out.dtype], args.partition_blocks,
+            ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
+    launches_per_step = 2  # decode kernel + merge kernel
+
+    def step():
+        code = fn(*argv)
+        if code != 0:
+            raise pa.PagedAttentionError(code, "pa_append_decode")
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    code, detail = pa.pa_check(pool)
+    assert code == 0, (pa.strerror(code), detail)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
+    t_wall = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record()
+        pa.pa_set_profile_events(kev[k][0], kev[k][1])
+        step()
+        ev[k][1].record()
+    pa.pa_set_profile_events(None, None)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clock_info = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    mean_ms = float(np.mean(step_ms))
+    kern_mean = float(np.mean(kern_ms))
+    code, detail = pa.pa_check(pool)
+    assert code == 0, (pa.strerror(code), detail)
+
+    # end to end through the public call: pinned host inputs in, output out
+    q_h = case.q.pin_memory(); kn_h = case.k_new.pin_memory(); vn_h = case.v_new.pin_memory()
+    bt_h = torch.from_numpy(tables).pin_memory(); sl_h = torch.from_numpy(dec_lens).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, bt_h, sl_h))
+    d2h = out_h.numel() * out_h.element_size()
+    KE = min(args.e2e_steps, K)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KE)]
+    torch.cuda.synchronize()
+    for k in range(KE):
+        flush.zero_()
+        eev[k][0].record()
+        q.copy_(q_h, non_blocking=True); k_new.copy_(kn_h, non_blocking=True)
+        v_new.copy_(vn_h, non_blocking=True); bt.copy_(bt_h, non_blocking=True)
+        sl.copy_(sl_h, non_blocking=True)
+        pa.pa_append_decode(pool, q, k_new, v_new, bt, sl, case.scale, out,
+                            partition_blocks=args.partition_blocks, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        eev[k][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
+
+    times = torch.tensor([mean_ms, kern_mean, e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    mean_ms, kern_mean, e2e_ms = times.tolist()
+    pool.close()
+    return dict(cfg=cfg, case=case, dec_lens=dec_lens, tables=tables, nbytes=nbytes, mean_ms=mean_ms,
+                p10=float(np.percentile(step_ms, 10)), p90=float(np.percentile(step_ms, 90)),
+                kern_ms=kern_mean, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, wall=wall, clocks=clock_info,
+                launches=launches_per_step * K, K=K, l2=l2)
+
+
+class OracleSample:
+    """The oracle, as it stands, on the first n (sequence, kv head) groups of
+    the step's workload (each group = its G query heads over the sequence's
+    appended cache).  Algorithmic bytes of a group: L_i * d * 2 (K, V) * 2."""
+
+    def __init__(self, cfg, case, tables, dec_lens, threads):
+        import oracle
+        self.oracle = oracle
+
+        def bits(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+        self.q = bits(case.q)
+        self.kp, self.vp = oracle.cache.append(bits(case.k_pool), bits(case.v_pool), bits(case.k_new),
+                                               bits(case.v_new), self._slots(tables, dec_lens))
+        self.cfg, self.case, self.tables, self.lens = cfg, case, tables, dec_lens
+        self.code = 0 if cfg.dtype == "fp16" else 1
+        self.threads = threads
+        self.G = cfg.n_q_heads // cfg.n_kv_heads
+        self.groups = len(dec_lens) * cfg.n_kv_heads
+
+    @staticmethod
+    def _slots(tables, lens):
+        pos = lens.astype(np.int64) - 1
+        return tables[np.arange(len(lens)), pos // 16].astype(np.int64) * 16 + pos % 16
+
+    def bytes_of(self, n):
+        seq = np.arange(n) // self.cfg.n_kv_heads
+        return int(np.sum(self.lens[seq])) * self.cfg.d_head * 2 * 2
+
+    def run(self, n):
+        rows = np.arange(n * self.G, dtype=np.int32)
+        t0 = time.perf_counter()
+        self.oracle.paged_decode(self.q, self.kp, self.vp, self.code, self.tables, self.lens, self.case.scale,
+                                 rows=rows, threads=self.threads)
+        return time.perf_counter() - t0
+
+    def size_for(self, seconds):
+        n1 = min(self.groups, max(1, 4 * self.threads))
+        t1 = self.run(n1)
+        n = int(n1 * seconds / max(t1, 1e-6))
+        return max(1, min(self.groups, n))
+
+    def describe(self, n):
+        toks = self.bytes_of(n) // (self.cfg.d_head * 4)
+        return (f"first {n} of {self.groups} (sequence, kv head) groups, {self.G} q heads each, "
+                f"{toks} token rows; fp64 C oracle, {self.threads} OpenMP threads")
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        torch.distributed.init_process_group(backend, device_id=torch.device("cuda", local)
+                                             if backend == "nccl" else None)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    r = run_ours(args, rank, world, local)
+    cfg, nb = r["cfg"], r["nbytes"]
+    peak, peak_kind = measured_peak()
+    value = nb["total"] * world / (r["mean_ms"] * 1e-3) / 1e9
+    achieved = nb["total"] / (r["kern_ms"] * 1e-3) / 1e9
+    traffic = traffic_record(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": r["K"],
+        "warmup": args.warmup,
+        "ms_per_step": round(r["mean_ms"], 5),
+        "us_per_step": round(r["mean_ms"] * 1e3, 2),
+        "us_per_step_p10_p90": [round(r["p10"] * 1e3, 2), round(r["p90"] * 1e3, 2)],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "fp16",
+        "data": "synthetic (seeded N(0,1) q/k/v, lengths and random block placement; no dataset)",
+        "config": {
+            "workload": cfg.name,
+            "batch_per_gpu": len(r["dec_lens"]),
+            "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "d_head": cfg.d_head,
+            "block_size": 16,
+            "lengths": "lognormal median 600 sigma 0.8 clip [16,8192] + 1 new token"
+            if cfg.key == 3 else str(cfg.lengths),
+            "tokens_attended": int(np.sum(r["dec_lens"])),
+            "pool_blocks": r["case"].num_blocks,
+            "step": "pa_append_decode (fused append + balanced split-KV decode + LSE merge)",
+            "partition_blocks": args.partition_blocks,
+            "l2": f"flushed before every timed step (write of {2 * r['l2'] >> 20} MiB)",
+            "bytes_per_step": nb,
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "decode_kernel (fused append + split decode)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "kernel_us": round(r["kern_ms"] * 1e3, 2),
+            "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+        },
+        "e2e": {
+            "value": round(nb["total"] * world / (r["e2e_ms"] * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "us_per_step": round(r["e2e_ms"] * 1e3, 2),
+            "h2d_bytes_per_step": r["h2d"],
+            "d2h_bytes_per_step": r["d2h"],
+        },
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0))
+        smp = OracleSample(cfg, r["case"], r["tables"], r["dec_lens"], threads)
+        n = smp.size_for(args.cpu_seconds)
+        dt = smp.run(n)
+        line["cpu_baseline"] = {"value": round(smp.bytes_of(n) / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": smp.describe(n) + f", {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle as the reference arm: each step runs it on a bounded
+    sample of the workload, sized so that warm-up and timed steps together
+    take about two minutes; rank 0 alone runs and prints."""
+    if rank != 0:
+        return
+    from oracle.allocator import ReferenceAllocator
+    from workloads import CONFIGS, build_tables, make_case
+    cfg = CONFIGS[args.workload]
+    case = make_case(cfg)
+    tables, slots, cows, dec_lens = build_tables(case, ReferenceAllocator(case.num_blocks, 16, case.free_order))
+    threads = len(os.sched_getaffinity(0))
+    smp = OracleSample(cfg, case, tables, dec_lens, threads)
+    n = smp.size_for(min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        smp.run(n)
+    dts = [smp.run(n) for _ in range(args.steps)]
+    dt = float(np.mean(dts)) if dts else smp.run(n)
+    value = smp.bytes_of(n) / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": cfg.name, "sample": smp.describe(n)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": smp.describe(n)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

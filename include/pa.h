@@ -135,15 +135,20 @@ int pa_decode(pa_pool_t pool, const void* q, const int32_t* block_tables,
               void* stream);
 
 /* Workspace bytes that pa_decode_split / pa_append_decode need for these
- * sizes (partition_blocks as passed to them; 0 = automatic choice). */
-size_t pa_decode_workspace_bytes(int num_seqs, int n_q_heads,
+ * sizes on this pool's device (partition_blocks as passed to them; 0 = the
+ * balanced automatic split).  Host only; returns 0 for invalid sizes. */
+size_t pa_decode_workspace_bytes(pa_pool_t pool, int num_seqs, int n_q_heads,
                                  int max_blocks_per_seq, int partition_blocks);
 
-/* Split-KV decode: each sequence's logical blocks are cut into partitions of
- * partition_blocks blocks (0 = chosen from the sizes and the SM count); each
- * (sequence, kv head, partition) is one work unit that writes its running
- * max m, sum l and unnormalised output o in fp32 to the workspace, and a
- * second kernel merges the partitions by log-sum-exp:
+/* Split-KV decode.  partition_blocks > 0: each sequence's logical blocks are
+ * cut into partitions of partition_blocks blocks, and each (sequence, kv head,
+ * partition) is one work unit.  partition_blocks == 0: the tiles of all
+ * (sequence, kv head) pairs, laid end to end, are cut into equal ranges, one
+ * per CTA of a persistent grid sized to the GPU, so any length mix is spread
+ * evenly; a pair cut by a range boundary becomes several units.  A unit that
+ * does not cover its whole pair writes its running max m, sum l and
+ * unnormalised output o in fp32 to the workspace, and a second kernel merges
+ * them by log-sum-exp:
  *   M = max_p m_p,  out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
  * The result equals pa_decode's up to rounding.  Sequences with a single
  * partition are written directly.  workspace: device, at least
@@ -177,6 +182,14 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
  * sharing with copy-on-write). */
 int pa_copy_blocks(pa_pool_t pool, const int32_t* src, const int32_t* dst,
                    int n, void* stream);
+
+/* Profiling hook.  When both events are non-NULL (cudaEvent_t passed as
+ * void*), every later pa_decode / pa_decode_split / pa_append_decode call
+ * records `start` on its stream right before its main decode kernel and
+ * `stop` right after it (so the merge kernel is outside the pair).  NULL, NULL
+ * turns the hook off.  Process-wide and not thread-safe; meant for
+ * benchmarks that time the dominant kernel alone. */
+int pa_set_profile_events(void* start, void* stop);
 
 /* Synchronises `stream`, reads and clears the pool's device error word.
  * Returns PA_OK, PA_ERR_DEVICE_CHECK or PA_ERR_TIMEOUT; *detail (may be NULL)

@@ -1,0 +1,50 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+// One pool: K and V arrays [num_blocks][n_kv_heads][16][128] plus a device
+// error word.  Fixed-size physical blocks as in "Serving" 23.4.
+struct pa_pool {
+  int num_blocks;
+  int n_kv_heads;
+  int dtype;          // PA_FP16 | PA_BF16
+  int device;
+  void* k;            // device
+  void* v;            // device
+  size_t bytes;       // bytes of one of k / v
+  long long* err;     // device: [0] = status code, [1] = detail
+};
+
+namespace pa {
+
+constexpr int kBlock = PA_BLOCK_SIZE;     // tokens per block
+constexpr int kHeadDim = PA_HEAD_DIM;     // elements per K/V row
+constexpr int kRowBytes = kHeadDim * 2;   // one 16-bit row: 256 B
+constexpr int kTileBytes = kBlock * kRowBytes;  // one (block, head) tile: 4 KiB
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Maps a CUDA error to a status (and clears sticky-free launch errors).
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Records the first device-side error: code in err[0] (0 -> code), detail in
+// err[1].  Later errors are dropped.
+__device__ inline void record_error(long long* err, long long code, long long detail) {
+  if (atomicCAS(reinterpret_cast<unsigned long long*>(err), 0ull,
+                static_cast<unsigned long long>(code)) == 0ull) {
+    atomicExch(reinterpret_cast<unsigned long long*>(err + 1),
+               static_cast<unsigned long long>(detail));
+  }
+}
+
+// Number of SMs of the current device (cached per device).
+int sm_count(int device);
+
+// Wait limit for bounded in-kernel waits, in nanoseconds.
+long long wait_limit_ns();
+
+}  // namespace pa

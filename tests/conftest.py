@@ -27,3 +27,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_library():
+    """Builds the CUDA library (sm_103a) and the oracle once if they are stale."""
+    from paged_kv_cache_227_gb300 import build as libbuild
+    libbuild.build()
+    import oracle.attention
+    oracle.attention.build()
