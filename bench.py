@@ -203,7 +203,7 @@ def run_ours(args, rank, world, local):
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    pa.pa_profile_start(K)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -212,17 +212,16 @@ def run_ours(args, rank, world, local):
     for k in range(K):
         flush.zero_()
         ev[k][0].record()
-        pa.pa_set_profile_events(kev[k][0], kev[k][1])
         step()
         ev[k][1].record()
-    pa.pa_set_profile_events(None, None)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     clock_info = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    kern_ms = pa.pa_profile_stop(K)
+    assert len(kern_ms) == K, "every timed step must record its decode kernel"
     mean_ms = float(np.mean(step_ms))
     kern_mean = float(np.mean(kern_ms))
     code, detail = pa.pa_check(pool)

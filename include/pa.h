@@ -183,13 +183,17 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
 int pa_copy_blocks(pa_pool_t pool, const int32_t* src, const int32_t* dst,
                    int n, void* stream);
 
-/* Profiling hook.  When both events are non-NULL (cudaEvent_t passed as
- * void*), every later pa_decode / pa_decode_split / pa_append_decode call
- * records `start` on its stream right before its main decode kernel and
- * `stop` right after it (so the merge kernel is outside the pair).  NULL, NULL
- * turns the hook off.  Process-wide and not thread-safe; meant for
- * benchmarks that time the dominant kernel alone. */
-int pa_set_profile_events(void* start, void* stop);
+/* Kernel timing for benchmarks.  pa_profile_start(capacity) creates
+ * `capacity` pairs of CUDA events on the current device; each later
+ * pa_decode / pa_decode_split / pa_append_decode call (until `capacity` calls
+ * have been recorded) records one pair on its stream, right before and right
+ * after its main decode kernel, so a merge kernel is outside the pair.
+ * pa_profile_stop(ms, cap) waits for the recorded pairs, writes up to cap
+ * elapsed times in milliseconds to ms (host), releases the events and returns
+ * how many pairs were recorded (or a negative status).  Process-wide, not
+ * thread-safe; starting again discards an unfinished profile. */
+int pa_profile_start(int capacity);
+int pa_profile_stop(float* ms, int cap);
 
 /* Synchronises `stream`, reads and clears the pool's device error word.
  * Returns PA_OK, PA_ERR_DEVICE_CHECK or PA_ERR_TIMEOUT; *detail (may be NULL)

@@ -51,7 +51,8 @@ def _load():
         "pa_append_decode": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
         "pa_copy_blocks": (i32, [vp, vp, vp, i32, vp]),
         "pa_check": (i32, [vp, vp, ctypes.POINTER(i64)]),
-        "pa_set_profile_events": (i32, [vp, vp]),
+        "pa_profile_start": (i32, [i32]),
+        "pa_profile_stop": (i32, [ctypes.POINTER(f32), i32]),
         "pa_strerror": (ctypes.c_char_p, [i32]),
         "pa_alloc_create": (i32, [i32, i32, vp, ctypes.POINTER(vp)]),
         "pa_alloc_destroy": (i32, [vp]),
@@ -233,12 +234,19 @@ def pa_copy_blocks(pool, src, dst, stream=None):
            "pa_copy_blocks")
 
 
-def pa_set_profile_events(start=None, stop=None):
-    """Record torch.cuda.Event `start`/`stop` around the main decode kernel of
-    every later decode call (None, None turns it off)."""
-    s = ctypes.c_void_p(start.cuda_event) if start is not None else None
-    e = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
-    _check(lib.pa_set_profile_events(s, e), "pa_set_profile_events")
+def pa_profile_start(capacity):
+    """Time the main decode kernel of the next `capacity` decode calls."""
+    _check(lib.pa_profile_start(int(capacity)), "pa_profile_start")
+
+
+def pa_profile_stop(cap=1 << 20):
+    """Milliseconds of each recorded decode kernel (list of floats)."""
+    import numpy as np
+    buf = np.zeros(max(1, cap), dtype=np.float32)
+    n = lib.pa_profile_stop(buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), cap)
+    if n < 0:
+        _check(n, "pa_profile_stop")
+    return buf[:min(n, cap)].tolist()
 
 
 def pa_check(pool, stream=None):

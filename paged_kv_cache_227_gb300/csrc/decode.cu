@@ -39,7 +39,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstddef>
 #include <mutex>
+#include <vector>
 
 #include "pa_internal.h"
 
@@ -304,21 +306,34 @@ struct PieceIter {
 // ---------------------------------------------------------------------------
 // Shared memory.
 // ---------------------------------------------------------------------------
+// Arrays read or written with 16-byte vector accesses come first and are
+// 16-byte aligned (checked below); the mbarriers need 8-byte alignment.
 template <int G>
 struct __align__(128) Smem {
   uint8_t stage[kStages][kStageBytes];
-  unsigned long long full[kStages];
+  __align__(16) float ow[kConsumerWarps][G][kHeadDim];
+  __align__(16) float pbuf[kConsumerWarps][kBlock][G <= 4 ? 4 : 8];
+  __align__(8) unsigned long long full[kStages];
   unsigned long long empty[kStages];
+  float mw[kConsumerWarps][G];
+  float lw[kConsumerWarps][G];
   int stage_blk[kStages];
   int issued[kStages];
   int consumed[kStages];
   int abort_flag;
-  float pbuf[kConsumerWarps][kBlock][G <= 4 ? 4 : 8];
-  float mw[kConsumerWarps][G];
-  float lw[kConsumerWarps][G];
-  float ow[kConsumerWarps][G][kHeadDim];
   int pfx[1];  // [B + 1], dynamic tail
 };
+
+template <int G>
+constexpr bool smem_layout_ok() {
+  return offsetof(Smem<G>, stage) == 0 && offsetof(Smem<G>, ow) % 16 == 0 &&
+         offsetof(Smem<G>, pbuf) % 16 == 0 && offsetof(Smem<G>, full) % 8 == 0 &&
+         offsetof(Smem<G>, empty) % 8 == 0 && kStageBytes % 128 == 0;
+}
+static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() &&
+                  smem_layout_ok<4>() && smem_layout_ok<5>() && smem_layout_ok<6>() &&
+                  smem_layout_ok<7>() && smem_layout_ok<8>(),
+              "shared-memory layout breaks a vector or mbarrier alignment");
 
 template <int G>
 constexpr size_t smem_bytes(int B) {
@@ -759,7 +774,15 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params P) {
 // ---------------------------------------------------------------------------
 // Host side: dispatch over (G, dtype, fused).
 // ---------------------------------------------------------------------------
-static cudaEvent_t g_profile_start = nullptr, g_profile_stop = nullptr;
+// Library-owned timing events (pa_profile_start / pa_profile_stop).
+static std::vector<cudaEvent_t> g_prof_events;  // [2 * capacity]
+static int g_prof_next = 0;
+
+static void profile_release() {
+  for (cudaEvent_t e : g_prof_events) cudaEventDestroy(e);
+  g_prof_events.clear();
+  g_prof_next = 0;
+}
 
 template <int G, bool kBf16, bool kFused>
 static int occupancy_for(int B) {
@@ -804,11 +827,14 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
     grid = parts < slots ? parts : slots;
   }
   if (grid < 1) grid = 1;
-  cudaEvent_t ev_start = g_profile_start, ev_stop = g_profile_stop;
-  if (ev_start && ev_stop && cudaEventRecord(ev_start, stream) != cudaSuccess) return PA_ERR_CUDA;
+  const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
+  if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
   decode_kernel<G, kBf16, kFused>
       <<<static_cast<int>(grid), kThreads, smem_bytes<G>(B_smem), stream>>>(P);
-  if (ev_start && ev_stop && cudaEventRecord(ev_stop, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (timed) {
+    if (cudaEventRecord(g_prof_events[2 * g_prof_next + 1], stream) != cudaSuccess) return PA_ERR_CUDA;
+    ++g_prof_next;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (P.sched != SCHED_SEGMENT) {
@@ -908,10 +934,31 @@ using namespace pa;
 
 extern "C" {
 
-int pa_set_profile_events(void* start, void* stop) {
-  g_profile_start = static_cast<cudaEvent_t>(start);
-  g_profile_stop = static_cast<cudaEvent_t>(stop);
+int pa_profile_start(int capacity) {
+  if (capacity < 0) return PA_ERR_INVALID;
+  profile_release();
+  g_prof_events.resize(2 * static_cast<size_t>(capacity), nullptr);
+  for (auto& e : g_prof_events) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      profile_release();
+      return PA_ERR_CUDA;
+    }
+  }
   return PA_OK;
+}
+
+int pa_profile_stop(float* ms, int cap) {
+  if (cap < 0 || (cap > 0 && !ms)) return PA_ERR_INVALID;
+  int n = g_prof_next;
+  int status = PA_OK;
+  for (int k = 0; k < n && k < cap; ++k) {
+    if (cudaEventSynchronize(g_prof_events[2 * k + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms[k], g_prof_events[2 * k], g_prof_events[2 * k + 1]) != cudaSuccess)
+      status = PA_ERR_CUDA;
+  }
+  profile_release();
+  return status == PA_OK ? n : status;
 }
 
 int pa_decode(pa_pool_t p, const void* q, const int32_t* block_tables, int max_blocks_per_seq,

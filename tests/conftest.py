@@ -32,7 +32,7 @@ def pytest_collection_modifyitems(config, items):
 @pytest.fixture(scope="session", autouse=True)
 def _built_library():
     """Builds the CUDA library (sm_103a) and the oracle once if they are stale."""
-    from paged_kv_cache_227_gb300 import build as libbuild
-    libbuild.build()
+    import __graft_entry__
+    __graft_entry__._libbuild().build()
     import oracle.attention
     oracle.attention.build()

@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from paged_kv_cache_227_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._libbuild().build()
     return ctypes.CDLL(path)
 
 

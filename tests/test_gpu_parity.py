@@ -201,27 +201,34 @@ def test_block_permutation_gives_bit_identical_output(pa):
     assert torch.equal(out1, out2)
 
 
+def unshare(c):
+    """Host side of the shared-prefix test: every sequence after the first gets
+    private copies (appended to the pool) of the blocks it shares."""
+    shared = {b for b in range(c.case.num_blocks) if c.alloc.refcount[b] > 1}
+    assert shared, "config 4 must share blocks"
+    tables = c.tables.copy()
+    extra_k, extra_v = [], []
+    n = c.case.num_blocks
+    for i in range(1, len(c.dec_lens)):
+        for j, b in enumerate(tables[i].tolist()):
+            if b in shared:
+                extra_k.append(c.kp[b]); extra_v.append(c.vp[b])
+                tables[i, j] = n
+                n += 1
+    kp = np.concatenate([c.kp, np.stack(extra_k)])
+    vp = np.concatenate([c.vp, np.stack(extra_v)])
+    return kp, vp, tables, n
+
+
 def test_shared_prefix_equals_unshared_copy(pa):
     """Sequences sharing prefix blocks give bit-identical results to the same
     sequences with private copies of those blocks."""
     c = GpuCase(4, lens=[2100, 2500, 2048, 3000, 2200, 2600])
     out_shared = _run(pa, c, "split", c.pool())
-    # give every sharer private copies of the shared blocks
-    shared = sorted({b for b in range(c.case.num_blocks) if c.alloc.refcount[b] > 1})
-    assert shared, "config 4 must share blocks"
-    free = sorted(set(range(c.case.num_blocks)) - set(int(b) for b in c.tables[c.tables >= 0])
-                  - set(c.alloc.tables[len(c.dec_lens)]))
-    tables = c.tables.copy()
-    kp, vp = c.kp.copy(), c.vp.copy()
-    it = iter(free)
-    for i in range(1, len(c.dec_lens)):
-        for j, b in enumerate(tables[i]):
-            if b in shared:
-                nb = next(it)
-                kp[nb], vp[nb] = c.kp[b], c.vp[b]
-                tables[i, j] = nb
+    kp, vp, tables, n = unshare(c)
     c.kp, c.vp, c.tables = kp, vp, tables
-    out_copy = _run(pa, c, "split", c.pool(), after_append=False)
+    c.case.num_blocks = n
+    out_copy = _run(pa, c, "split", c.pool())
     assert torch.equal(out_shared, out_copy)
 
 

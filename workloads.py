@@ -99,7 +99,8 @@ def pool_size(cfg, lens):
     if cfg.shared_prefix:
         # children share the parent's prefix blocks; count them once
         shared = cfg.shared_prefix // BLOCK_SIZE
-        need = need - shared * len(cfg.shared_children) + shared
+        children = sum(1 for i in cfg.shared_children if i < len(lens))
+        need = need - shared * children + shared
     return int(math.ceil(cfg.pool_factor * need))
 
 
