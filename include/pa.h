@@ -147,14 +147,17 @@ size_t pa_decode_workspace_bytes(pa_pool_t pool, int num_seqs, int n_q_heads,
  * per CTA of a persistent grid sized to the GPU, so any length mix is spread
  * evenly; a pair cut by a range boundary becomes several units.  A unit that
  * does not cover its whole pair writes its running max m, sum l and
- * unnormalised output o in fp32 to the workspace, and a second kernel merges
- * them by log-sum-exp:
+ * unnormalised output o in fp32 to the workspace and counts itself done on
+ * the pair's counter; the CTA that finishes the pair's last unit merges the
+ * partial results by log-sum-exp in the same launch:
  *   M = max_p m_p,  out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
- * The result equals pa_decode's up to rounding.  Sequences with a single
- * partition are written directly.  workspace: device, at least
- * pa_decode_workspace_bytes(...) bytes, 16-byte aligned, caller-owned; its
- * contents need no initialisation and are garbage afterwards.  Calls that
- * share a workspace must not overlap on the GPU. */
+ * The result equals pa_decode's up to rounding.  Pairs covered by a single
+ * unit are written directly.  workspace: device, at least
+ * pa_decode_workspace_bytes(...) bytes, 16-byte aligned, caller-owned.  It
+ * must be zero-filled before its first use; every call that returns PA_OK and
+ * completes on the GPU leaves its counters at zero again (after a device
+ * error, zero it again).  Calls that share a workspace must not overlap on
+ * the GPU. */
 int pa_decode_split(pa_pool_t pool, const void* q, const int32_t* block_tables,
                     int max_blocks_per_seq, const int32_t* seq_lens,
                     int num_seqs, int n_q_heads, float scale, void* out,

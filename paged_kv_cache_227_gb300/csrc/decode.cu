@@ -4,8 +4,9 @@
 // fixed-size 16-token blocks found through a per-sequence block table
 // ("Serving", section 23.4 Paged Attention).  Decode reads the whole cache
 // for one token per sequence, so it is bound by HBM bandwidth ("Serving",
-// section 23.2 Prefill and Decode); the design keeps every K/V byte read
-// exactly once and keeps enough bytes in flight to saturate HBM3e.
+// section 23.2 Prefill and Decode); the design reads every K/V byte exactly
+// once, keeps enough bytes in flight to saturate HBM3e, and keeps the SM's
+// instruction issue far below the memory time.
 //
 // Work decomposition.  A segment is one (sequence i, kv head h) pair: its
 // nb_i = ceil(L_i/16) tiles of 16 tokens x 128 dims (4 KiB each for K and
@@ -15,27 +16,35 @@
 // range of a segment's tiles) given by one of three schedules:
 //   SEGMENT    whole segments, strided over CTAs (no workspace);
 //   LEAN       the concatenated tile stream of all segments cut into equal
-//              per-CTA ranges (perfect balance for any length mix); a segment
-//              cut by a range boundary leaves partial results;
+//              per-CTA ranges (even load for any length mix); a segment cut
+//              by a range boundary leaves partial results;
 //   PARTITION  fixed partitions of `partition_blocks` tiles per segment.
-// Partial results (running max m, sum l, unnormalised o, fp32) are merged by
-// a log-sum-exp kernel.
+// A piece that does not cover its whole segment writes a partial record
+// (running max m, sum l, unnormalised o, fp32) and bumps the segment's
+// counter; the CTA that completes the count merges the records by
+// log-sum-exp and writes the output, then resets the counter to zero.
 //
-// CTA layout: 4 consumer warps + 1 producer warp.  The producer walks the
-// block table and streams each (block, head) K and V tile (contiguous in the
-// [block][head][16][128] pool) into an 8-stage shared-memory ring with
-// cp.async.bulk, completion tracked by mbarriers.  Tile n of the CTA's stream
-// goes to stage n % 8 and is consumed by warp n % 4, which runs the online
-// softmax over its own tiles; the 4 warps' states are merged per piece.
+// CTA layout: 4 consumer warps + 1 producer warp, two CTAs per SM.  The
+// producer walks the block table and streams each (block, head) K and V tile
+// into a shared-memory ring of S = 12 stages (8 for G > 4) with TMA tensor
+// loads (two 16-row x 128-byte boxes per tile, 128-byte swizzle), completion
+// tracked by mbarriers.  Tile n of the CTA's stream goes to stage n % S and
+// is consumed by warp n % 4, which runs the online softmax over its own
+// tiles; the warps' states are merged at the end of each piece.
 //
-// Per tile a consumer warp computes, in fp32:
-//   scores  s[t][g] = <q_g * scale * log2(e), K[t]>   (8 lanes per token row,
-//           partial dots reduced across lanes by a reduce-scatter butterfly)
-//   online softmax with a lazily moved running max (rescale only when a new
-//           max exceeds the old by 2^8), p = 2^(s - m)
-//   o[g][:] += sum_t p[t][g] V[t][:]                    (16 lanes per row)
-// Positions t >= L are masked by select, never by multiplying, so padding or
-// stale slots (even NaN) never reach the output.
+// Per tile a consumer warp runs two small tensor-core contractions with
+// mma.sync m16n8k16 (fp32 accumulate): the 16 MMA rows are the query heads
+// of the group (G <= 8, the rest zero), so
+//   S[g][t] = q_g . K[t]          2 n-tiles of 8 tokens x 8 k-steps of 16 dims
+//   O[g][:] += P[g][t] V[t][:]    16 n-tiles of 8 dims x 1 k-step of 16 tokens
+// The S accumulator fragments are exactly the A fragments of the second
+// product, so P never leaves registers.  P is split into a bf16/fp16 high
+// part and the rounded remainder, and both are multiplied, which keeps the
+// weights accurate to ~2^-17.  Softmax runs in fp32 in the log2 domain with
+// a lazily moved running max (rescale only when a new max exceeds the old by
+// 2^8).  Positions t >= L are masked by select on S and their V rows are
+// zeroed in shared memory, so padding or stale slots (even NaN) never reach
+// the output.  ldmatrix reads the swizzled tiles without bank conflicts.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,19 +56,28 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;
-constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-constexpr int kMaxSplitSeqs = 8192;          // sequences per split launch
+constexpr int kMaxSplitSeqs = 4096;  // sequences per split launch (prefix in shared memory)
 constexpr int kMaxCtasPerSm = 4;
-constexpr int kLeanMinBlocks = 8;            // smallest LEAN range per CTA
+constexpr int kLeanMinBlocks = 8;    // smallest LEAN range per CTA
+constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 
 enum { SCHED_SEGMENT = 0, SCHED_LEAN = 1, SCHED_PARTITION = 2 };
 
+// Compile-time shape of the kernel: 4 consumer warps; 12 ring stages for
+// G <= 4 and 8 for larger groups (whose merge buffer is bigger), so that two
+// CTAs fit in an SM's shared memory either way.
+template <int G>
+struct Shape {
+  static constexpr int NW = 4;                          // consumer warps (+1 producer)
+  static constexpr int kStages = G <= 4 ? 3 * NW : 2 * NW;
+  static constexpr int kThreads = (NW + 1) * 32;
+};
+
 struct Params {
+  CUtensorMap tmap_k;       // token-row views of the pools (see pa_pool)
+  CUtensorMap tmap_v;
   const uint16_t* q;        // [B][Hq][128]
   const uint16_t* k_pool;   // [N][Hkv][16][128]
   const uint16_t* v_pool;
@@ -69,6 +87,7 @@ struct Params {
   const int32_t* seq_lens;  // [B]
   void* out;                // [B][Hq][128]
   float* ws;                // partial records
+  int* counters;            // [B][Hkv] pieces finished per segment (zero between calls)
   long long* err;
   long long num_blocks;
   int max_blocks;
@@ -125,16 +144,20 @@ __device__ __forceinline__ long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+template <int NT>
 __device__ __forceinline__ int consumers_sync_or(int pred) {
   int r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 2, 128, p;\n\t"
+      "bar.red.or.pred q, 2, %2, p;\n\t"
       "selp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred)
+      : "r"(pred), "n"(NT)
       : "memory");
   return r;
 }
@@ -161,22 +184,72 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-// 16-bit -> fp32 for 8 packed elements.
+
+// TMA tensor load of one box (x = element column, y = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A B + D for m16n8k16 with rows 8..15 of A zero: only the accumulator
+// of row group (lane / 4) is kept (d0, d1); a0/a2 are the row's k 0-7 / 8-15
+// pairs, b0/b1 the column's k 0-7 / 8-15 pairs.
 template <bool kBf16>
-__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (kBf16) {
-      f[2 * k] = __uint_as_float(w[k] << 16);
-      f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    } else {
-      __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
-      float2 t = __half22float2(h);
-      f[2 * k] = t.x;
-      f[2 * k + 1] = t.y;
-    }
+__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
+                                          uint32_t b1) {
+  float j0, j1;
+  const uint32_t z = 0;
+  const float fz = 0.f;
+  if (kBf16)
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d0), "=f"(d1), "=f"(j0), "=f"(j1)
+        : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(fz), "f"(fz));
+  else
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d0), "=f"(d1), "=f"(j0), "=f"(j1)
+        : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(fz), "f"(fz));
+}
+// Two floats -> packed 16-bit pair (x in the low half), and the rounding
+// remainders of the pair as a second packed pair.
+template <bool kBf16>
+__device__ __forceinline__ void split_pack(float x, float y, uint32_t& hi, uint32_t& lo) {
+  if (kBf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+  } else {
+    __half2 h = __floats2half2_rn(x, y);
+    float2 hf = __half22float2(h);
+    __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
   }
+}
+// Byte offset of 16-byte chunk c (0..15) of row r in a tile stored as two
+// 128-byte-swizzled boxes [16 rows][64 elements].
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ void store_out(void* out, long long idx, float x, int out_dtype) {
@@ -198,6 +271,12 @@ __device__ __forceinline__ int clamp_len(const Params& P, int i) {
   return L;
 }
 
+__device__ __forceinline__ long long lean_per(const Params& P, const int* pfx) {
+  long long T = static_cast<long long>(P.Hkv) * pfx[P.B];
+  long long per = (T + P.lean_grid - 1) / P.lean_grid;
+  return per < kLeanMinBlocks ? kLeanMinBlocks : per;
+}
+
 // ---------------------------------------------------------------------------
 // Piece enumeration: every thread of the CTA walks the same list.
 // ---------------------------------------------------------------------------
@@ -210,10 +289,8 @@ struct Piece {
 struct PieceIter {
   const Params& P;
   const int* pfx;  // shared: exclusive prefix over sequences (LEAN: tiles, PARTITION: partitions)
-  // SEGMENT / PARTITION cursor
-  long long x, x_end;
-  // LEAN cursor
-  long long cur, end;
+  long long x, x_end;        // SEGMENT / PARTITION cursor
+  long long cur, end;        // LEAN cursor
   int li, lh, lj;
   bool first;
 
@@ -221,12 +298,11 @@ struct PieceIter {
     first = true;
     if (P.sched == SCHED_LEAN) {
       long long T = static_cast<long long>(P.Hkv) * pfx[P.B];
-      long long per = (T + P.lean_grid - 1) / P.lean_grid;
-      if (per < kLeanMinBlocks) per = kLeanMinBlocks;
+      long long per = lean_per(P, pfx);
       cur = per * blockIdx.x;
       end = cur + per < T ? cur + per : T;
       if (cur < end) {
-        // largest i with Hkv*pfx[i] <= cur
+        // largest i with Hkv*pfx[i] <= cur (never an empty sequence)
         int lo = 0, hi = P.B - 1;
         while (lo < hi) {
           int mid = (lo + hi + 1) >> 1;
@@ -303,56 +379,88 @@ struct PieceIter {
   }
 };
 
+// Records of segment (i, h): how many, and the index of the k-th.
+struct SegmentRecords {
+  long long c0, s0, per, base;
+  int count;
+  __device__ SegmentRecords(const Params& P, const int* pfx, int i, int h) {
+    if (P.sched == SCHED_LEAN) {
+      int nb = pfx[i + 1] - pfx[i];
+      per = lean_per(P, pfx);
+      s0 = static_cast<long long>(P.Hkv) * pfx[i] + static_cast<long long>(h) * nb;
+      c0 = s0 / per;
+      count = static_cast<int>((s0 + nb - 1) / per - c0 + 1);
+      base = 0;
+    } else {
+      count = pfx[i + 1] - pfx[i];
+      base = static_cast<long long>(pfx[i]) * P.Hkv + h;
+      c0 = s0 = per = 0;
+    }
+  }
+  __device__ long long at(const Params& P, int k) const {
+    if (P.sched == SCHED_LEAN) return 2 * (c0 + k) + ((k == 0 && s0 > c0 * per) ? 1 : 0);
+    return base + static_cast<long long>(k) * P.Hkv;
+  }
+};
+
+
 // ---------------------------------------------------------------------------
-// Shared memory.
+// Shared memory.  The ring comes first at a 1024-byte aligned base (the
+// 128-byte swizzle of TMA boxes needs it); the mbarriers need 8 bytes.
 // ---------------------------------------------------------------------------
-// Arrays read or written with 16-byte vector accesses come first and are
-// 16-byte aligned (checked below); the mbarriers need 8-byte alignment.
 template <int G>
-struct __align__(128) Smem {
-  uint8_t stage[kStages][kStageBytes];
-  __align__(16) float ow[kConsumerWarps][G][kHeadDim];
-  __align__(16) float pbuf[kConsumerWarps][kBlock][G <= 4 ? 4 : 8];
-  __align__(8) unsigned long long full[kStages];
-  unsigned long long empty[kStages];
-  float mw[kConsumerWarps][G];
-  float lw[kConsumerWarps][G];
-  int stage_blk[kStages];
-  int issued[kStages];
-  int consumed[kStages];
+struct __align__(1024) Smem {
+  static constexpr int NW = Shape<G>::NW;
+  static constexpr int S = Shape<G>::kStages;
+  uint8_t stage[S][kStageBytes];
+  __align__(16) float ow[NW][G][kHeadDim];
+  __align__(8) unsigned long long full[S];
+  unsigned long long empty[S];
+  float mw[NW][G];
+  float lw[NW][G];
+  int stage_blk[S];
+  int issued[S];
+  int consumed[S];
   int abort_flag;
+  int merge_flag;
   int pfx[1];  // [B + 1], dynamic tail
 };
 
 template <int G>
 constexpr bool smem_layout_ok() {
   return offsetof(Smem<G>, stage) == 0 && offsetof(Smem<G>, ow) % 16 == 0 &&
-         offsetof(Smem<G>, pbuf) % 16 == 0 && offsetof(Smem<G>, full) % 8 == 0 &&
-         offsetof(Smem<G>, empty) % 8 == 0 && kStageBytes % 128 == 0;
+         offsetof(Smem<G>, full) % 8 == 0 && offsetof(Smem<G>, empty) % 8 == 0 &&
+         kStageBytes % 1024 == 0 && Shape<G>::kStages % Shape<G>::NW == 0;
 }
 static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() &&
                   smem_layout_ok<4>() && smem_layout_ok<5>() && smem_layout_ok<6>() &&
                   smem_layout_ok<7>() && smem_layout_ok<8>(),
-              "shared-memory layout breaks a vector or mbarrier alignment");
+              "shared-memory layout breaks a swizzle, vector or mbarrier alignment");
 
+// Dynamic shared memory to request: the struct, the prefix array, and slack
+// to align the base to 1024 bytes.
 template <int G>
 constexpr size_t smem_bytes(int B) {
-  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>(B + 1);
+  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>(B + 1) + 1024;
 }
-
 // ---------------------------------------------------------------------------
 // The decode kernel.
 // ---------------------------------------------------------------------------
 template <int G, bool kBf16, bool kFused>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem<G>& S = *reinterpret_cast<Smem<G>*>(smem_raw);
+__global__ void __launch_bounds__(Shape<G>::kThreads)
+    decode_kernel(const __grid_constant__ Params P) {
+  constexpr int NW = Shape<G>::NW;
+  constexpr int NS = Shape<G>::kStages;
+  constexpr int NT = NW * 32;  // consumer threads
+  extern __shared__ uint8_t smem_raw[];
+  Smem<G>& S = *reinterpret_cast<Smem<G>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   // --- set-up: barriers, prefix over sequences -----------------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(smem_addr(&S.full[s]), 1);
       mbar_init(smem_addr(&S.empty[s]), 1);
       S.issued[s] = 0;
@@ -389,9 +497,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
   __syncthreads();
 
   volatile int* abort_flag = &S.abort_flag;
-  const long long head_stride = static_cast<long long>(kBlock) * kHeadDim;  // elements per tile
 
-  if (warp == kConsumerWarps) {
+  if (warp == NW) {
     // ======================= producer warp =================================
     PieceIter it(P, S.pfx);
     Piece pc;
@@ -404,10 +511,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
         int my_blk = lane < cnt ? row[jb + lane] : 0;
         for (int k = 0; k < cnt; ++k, ++n) {
           int blk = __shfl_sync(0xffffffffu, my_blk, k);
-          int s = static_cast<int>(n % kStages);
+          int s = static_cast<int>(n % NS);
           if (lane == 0) {
-            if (n >= kStages)
-              ok = wait_phase(smem_addr(&S.empty[s]), static_cast<uint32_t>(((n / kStages) - 1) & 1),
+            if (n >= NS)
+              ok = wait_phase(smem_addr(&S.empty[s]), static_cast<uint32_t>(((n / NS) - 1) & 1),
                               abort_flag, P.wait_limit_ns, P.err, 1);
             if (ok) {
               bool valid = blk >= 0 && blk < P.num_blocks;
@@ -416,9 +523,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
               uint32_t fb = smem_addr(&S.full[s]);
               if (valid) {
                 mbar_arrive_expect_tx(fb, kStageBytes);
-                long long off = (static_cast<long long>(blk) * P.Hkv + pc.h) * head_stride;
-                bulk_copy_g2s(smem_addr(S.stage[s]), P.k_pool + off, kTileBytes, fb);
-                bulk_copy_g2s(smem_addr(S.stage[s] + kTileBytes), P.v_pool + off, kTileBytes, fb);
+                const int y = (blk * P.Hkv + pc.h) * kBlock;  // first token row of the tile
+                const uint32_t dst = smem_addr(S.stage[s]);
+                tma_load_2d(dst, &P.tmap_k, 0, y, fb);
+                tma_load_2d(dst + 2048, &P.tmap_k, kHeadDim / 2, y, fb);
+                tma_load_2d(dst + kTileBytes, &P.tmap_v, 0, y, fb);
+                tma_load_2d(dst + kTileBytes + 2048, &P.tmap_v, kHeadDim / 2, y, fb);
               } else {
                 record_error(P.err, PA_ERR_DEVICE_CHECK, static_cast<long long>(blk));
                 mbar_arrive(fb);
@@ -432,17 +542,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
     }
   } else {
     // ======================= consumer warps ================================
-    constexpr int TPL = G <= 4 ? 8 : 16;   // lanes per token row in the score phase
-    constexpr int CH = 16 / TPL;           // 16-byte chunks per lane
-    constexpr int TPP = 32 / TPL;          // tokens per pass
-    constexpr int NP = kBlock / TPP;       // passes per tile
-    constexpr int PB = G <= 4 ? 4 : 8;     // pbuf row stride
-    const int cg = lane % TPL;
-    const int ts = lane / TPL;
-    const int kq = (lane >> 1) & (NP - 1);  // pass index this lane owns after the reduction
-    const int tq = kq * TPP + ts;           // token this lane owns after the reduction
-    const int c16 = lane & 15;              // value phase: chunk
-    const int r16 = lane >> 4;              // value phase: token parity
+    const int gq = lane >> 2;  // MMA row group = query head of the group this lane holds
+    const int tq = lane & 3;   // thread in the row group
+    const int tid = threadIdx.x;
+    // ldmatrix row addresses: lane group lm supplies matrix lm, row lr
+    const int lm = lane >> 3, lr = lane & 7;
+    const int k_tok = lr + 8 * (lm >> 1), k_cadd = lm & 1;  // K: [tok 0-7 | 8-15] x [chunk +0 | +1]
+    const int v_tok = lr + 8 * (lm & 1), v_cadd = lm >> 1;  // V: [tok 0-7 | 8-15] per chunk, transposed
+
+    // zero rows of empty sequences (split schedules; SEGMENT pieces write them)
+    if (P.sched != SCHED_SEGMENT) {
+      for (int i = blockIdx.x; i < P.B; i += gridDim.x) {
+        if (S.pfx[i + 1] != S.pfx[i]) continue;
+        for (int x = tid; x < P.Hq * kHeadDim; x += NT)
+          store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
+      }
+    }
 
     PieceIter it(P, S.pfx);
     Piece pc;
@@ -452,36 +567,32 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
       const long long n0 = n;
       const int nblk = pc.j1 - pc.j0;
       n += nblk;
-      // query group of this piece, pre-scaled into log2 units
-      float qf[G][CH][8];
+      // A fragments of the query group (row gq; rows >= G are zero)
+      uint32_t qa[8][2];
+      if (gq < G) {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + gq) * kHeadDim);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const uint16_t* qrow = P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + g) * kHeadDim;
-#pragma unroll
-        for (int u = 0; u < CH; ++u) {
-          uint4 raw = *reinterpret_cast<const uint4*>(qrow + 8 * (cg + TPL * u));
-          unpack8<kBf16>(raw, qf[g][u]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) qf[g][u][e] *= P.qscale;
+        for (int ks = 0; ks < 8; ++ks) {
+          qa[ks][0] = qrow[8 * ks + tq];
+          qa[ks][1] = qrow[8 * ks + 4 + tq];
         }
-      }
-      float o[G][8];
-      float m_run[G], l_run[G];
+      } else {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        m_run[g] = -INFINITY;
-        l_run[g] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+        for (int ks = 0; ks < 8; ++ks) qa[ks][0] = qa[ks][1] = 0u;
       }
+      float o[16][2];
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = 0.f;
+      float m_run = -INFINITY, l_run = 0.f;
       const int nb_total = (pc.L + kBlock - 1) / kBlock;
 
       // first tile of this warp in the piece
-      int first = static_cast<int>((warp - (n0 % kConsumerWarps) + kConsumerWarps) % kConsumerWarps);
-      for (int b = first; ok && b < nblk; b += kConsumerWarps) {
+      int first = static_cast<int>((warp - (n0 % NW) + NW) % NW);
+      for (int b = first; ok && b < nblk; b += NW) {
         const long long nn = n0 + b;
-        const int s = static_cast<int>(nn % kStages);
-        const uint32_t parity = static_cast<uint32_t>((nn / kStages) & 1);
+        const int s = static_cast<int>(nn % NS);
+        const uint32_t parity = static_cast<uint32_t>((nn / NS) & 1);
         bool got = wait_phase(smem_addr(&S.full[s]), parity, abort_flag, P.wait_limit_ns, P.err, 2);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
@@ -492,160 +603,119 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
         const int blk = S.stage_blk[s];
         uint8_t* Ks = S.stage[s];
         uint8_t* Vs = Ks + kTileBytes;
+        const uint32_t ks_addr = smem_addr(Ks), vs_addr = smem_addr(Vs);
         const int valid_tokens = pc.L - j * kBlock < kBlock ? pc.L - j * kBlock : kBlock;
-        bool patched = false;
+        bool touched = false;
         if (blk >= 0) {
           if (kFused && j == nb_total - 1) {
             // the new token: use the caller's k_new/v_new for position L-1
             // and write it to its slot in the pool
             const int tn = (pc.L - 1) & (kBlock - 1);
+            const int c = lane & 15;
             const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
             const long long dst =
                 ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
             const uint16_t* from = (lane < 16 ? P.k_new : P.v_new) + src;
-            uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c16);
-            uint8_t* tile = lane < 16 ? Ks : Vs;
-            *reinterpret_cast<uint4*>(tile + tn * kRowBytes + 16 * c16) = val;
+            uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c);
+            *reinterpret_cast<uint4*>((lane < 16 ? Ks : Vs) + swz(tn, c)) = val;
             uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
-            *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = val;
-            patched = true;
-            __syncwarp();
+            *reinterpret_cast<uint4*>(pool_w + dst + 8 * c) = val;
+            touched = true;
           }
-          // ---- scores: partial dot products over this lane's chunks
-          float part[NP][G];
+          if (valid_tokens < kBlock) {
+            // V rows past the sequence end may hold anything (even NaN):
+            // zero them so that 0-weight rows contribute exactly 0
+            const int nz = (kBlock - valid_tokens) * 16;
+            for (int x = lane; x < nz; x += 32)
+              *reinterpret_cast<uint4*>(Vs + swz(valid_tokens + (x >> 4), x & 15)) = make_uint4(0, 0, 0, 0);
+            touched = true;
+          }
+          if (touched) __syncwarp();
+          // ---- S = Q K^T: 2 n-tiles (tokens 0-7, 8-15) x 8 k-steps
+          float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-          for (int k = 0; k < NP; ++k) {
-            const int t = k * TPP + ts;
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b00, b01, b10, b11;
+            ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), b00, b01, b10, b11);
+            mma_rows8<kBf16>(sc[0][0], sc[0][1], qa[ks][0], qa[ks][1], b00, b01);
+            mma_rows8<kBf16>(sc[1][0], sc[1][1], qa[ks][0], qa[ks][1], b10, b11);
+          }
+          // ---- online softmax of row gq over tokens 2tq, 2tq+1, 8+2tq, 9+2tq
+          float mx = -INFINITY;
 #pragma unroll
-            for (int g = 0; g < G; ++g) part[k][g] = 0.f;
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int u = 0; u < CH; ++u) {
-              uint4 raw = *reinterpret_cast<const uint4*>(Ks + t * kRowBytes + 16 * (cg + TPL * u));
-              float kf[8];
-              unpack8<kBf16>(raw, kf);
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) part[k][g] = fmaf(qf[g][u][e], kf[e], part[k][g]);
+            for (int c = 0; c < 2; ++c) {
+              const int t = 8 * nt + 2 * tq + c;
+              sc[nt][c] = t < valid_tokens ? sc[nt][c] * P.qscale : -INFINITY;
+              mx = fmaxf(mx, sc[nt][c]);
             }
-          }
-          // ---- reduce-scatter across the TPL lanes of a row
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          if (mx > m_run + kRescaleThreshold) {  // uniform within the row group
+            const float mn = fmaxf(m_run, mx);
+            const float alpha = fast_exp2(m_run - mn);
+            l_run *= alpha;
 #pragma unroll
-          for (int lvl = 0; (NP >> (lvl + 1)) >= 1; ++lvl) {
-            const int m = TPL >> (lvl + 1);
-            const int half = NP >> (lvl + 1);
-            const bool hi = (lane & m) != 0;
-#pragma unroll
-            for (int kk = 0; kk < half; ++kk)
-#pragma unroll
-              for (int g = 0; g < G; ++g) {
-                float keep = hi ? part[kk + half][g] : part[kk][g];
-                float send = hi ? part[kk][g] : part[kk + half][g];
-                part[kk][g] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-              }
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 1);
-          // ---- online softmax (log2 domain)
-          const bool tvalid = tq < valid_tokens;
-          float sc[G], bm[G];
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            sc[g] = tvalid ? part[0][g] : -INFINITY;
-            bm[g] = sc[g];
-#pragma unroll
-            for (int msk = 2; msk < 32; msk <<= 1)
-              bm[g] = fmaxf(bm[g], __shfl_xor_sync(0xffffffffu, bm[g], msk));
-          }
-          bool grow = false;
-#pragma unroll
-          for (int g = 0; g < G; ++g) grow |= bm[g] > m_run[g] + kRescaleThreshold;
-          if (grow) {  // warp-uniform
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float mn = fmaxf(m_run[g], bm[g]);
-              float alpha = fast_exp2(m_run[g] - mn);
-              l_run[g] *= alpha;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[g][e] *= alpha;
-              m_run[g] = mn;
+            for (int nt = 0; nt < 16; ++nt) {
+              o[nt][0] *= alpha;
+              o[nt][1] *= alpha;
             }
+            m_run = mn;
           }
-          float (*pb)[PB] = S.pbuf[warp];
-          if ((lane & 1) == 0) {
+          float p[2][2];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float p = fast_exp2(sc[g] - m_run[g]);
-              l_run[g] += p;
-              pb[tq][g] = p;
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              p[nt][c] = fast_exp2(sc[nt][c] - m_run);
+              l_run += p[nt][c];
             }
+          uint32_t ph0, pl0, ph1, pl1;  // A fragments of P: tokens 0-7 | 8-15, high and low parts
+          split_pack<kBf16>(p[0][0], p[0][1], ph0, pl0);
+          split_pack<kBf16>(p[1][0], p[1][1], ph1, pl1);
+          // ---- O += P V: 16 n-tiles of 8 dims, k = 16 tokens
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            uint32_t b0a, b1a, b0b, b1b;
+            ldsm_x4_trans(vs_addr + swz(v_tok, 2 * pp + v_cadd), b0a, b1a, b0b, b1b);
+            mma_rows8<kBf16>(o[2 * pp][0], o[2 * pp][1], ph0, ph1, b0a, b1a);
+            mma_rows8<kBf16>(o[2 * pp][0], o[2 * pp][1], pl0, pl1, b0a, b1a);
+            mma_rows8<kBf16>(o[2 * pp + 1][0], o[2 * pp + 1][1], ph0, ph1, b0b, b1b);
+            mma_rows8<kBf16>(o[2 * pp + 1][0], o[2 * pp + 1][1], pl0, pl1, b0b, b1b);
           }
-          __syncwarp();
-          // ---- o += p V
-#pragma unroll
-          for (int k = 0; k < kBlock / 2; ++k) {
-            const int t = 2 * k + r16;
-            if (t < valid_tokens) {
-              uint4 raw = *reinterpret_cast<const uint4*>(Vs + t * kRowBytes + 16 * c16);
-              float vf[8];
-              unpack8<kBf16>(raw, vf);
-              float p[PB];
-#pragma unroll
-              for (int g4 = 0; g4 < PB; g4 += 4) {
-                float4 pp = *reinterpret_cast<const float4*>(&pb[t][g4]);
-                p[g4] = pp.x; p[g4 + 1] = pp.y; p[g4 + 2] = pp.z; p[g4 + 3] = pp.w;
-              }
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[g][e] = fmaf(p[g], vf[e], o[g][e]);
-            }
-          }
-          __syncwarp();
         }
-        if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (touched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (lane == 0) {
           S.consumed[s] += 1;
           mbar_arrive(smem_addr(&S.empty[s]));
         }
       }
 
-      // ---- merge the 4 warps' states for this piece
+      // ---- merge the NW warps' states for this piece
+      float l = l_run;
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (gq < G) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
-        float l = l_run[g];
-#pragma unroll
-        for (int msk = 1; msk < 32; msk <<= 1) l += __shfl_xor_sync(0xffffffffu, l, msk);
-        l_run[g] = l;
-      }
-      if (lane < 16) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float4* dst = reinterpret_cast<float4*>(&S.ow[warp][g][8 * lane]);
-          dst[0] = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-          dst[1] = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
+        for (int nt = 0; nt < 16; ++nt)
+          *reinterpret_cast<float2*>(&S.ow[warp][gq][8 * nt + 2 * tq]) = make_float2(o[nt][0], o[nt][1]);
+        if (tq == 0) {
+          S.mw[warp][gq] = m_run;
+          S.lw[warp][gq] = l;
         }
       }
-      if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          S.mw[warp][g] = m_run[g];
-          S.lw[warp][g] = l_run[g];
-        }
-      }
-      consumers_sync();
-      const int e = threadIdx.x;  // 0..127: output element
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
+      consumers_sync<NT>();
+      for (int x = tid; x < G * kHeadDim; x += NT) {
+        const int g = x / kHeadDim, e = x % kHeadDim;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, S.mw[w][g]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, S.mw[w][g]);
         float Ls = 0.f, Os = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
+          for (int w = 0; w < NW; ++w) {
             float f = fast_exp2(S.mw[w][g] - M);
             Ls = fmaf(S.lw[w][g], f, Ls);
             Os = fmaf(S.ow[w][g][e], f, Os);
@@ -663,15 +733,44 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
           }
         }
       }
-      // all consumers agree whether to stop; also guards S.ow/mw/lw reuse
-      if (consumers_sync_or(ok ? 0 : 1)) break;
+      if (!pc.final_out) {
+        // ---- log-sum-exp merge by the CTA that completes the segment:
+        //   M = max_p m_p;  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p
+        __threadfence();
+        consumers_sync<NT>();
+        const SegmentRecords recs(P, S.pfx, pc.i, pc.h);
+        int* counter = P.counters + static_cast<long long>(pc.i) * P.Hkv + pc.h;
+        if (tid == 0) S.merge_flag = atomicAdd(counter, 1) == recs.count - 1;
+        consumers_sync<NT>();
+        if (S.merge_flag) {
+          __threadfence();
+          for (int x = tid; x < G * kHeadDim; x += NT) {
+            const int g = x / kHeadDim, e = x % kHeadDim;
+            float M = -INFINITY;
+            for (int k = 0; k < recs.count; ++k)
+              M = fmaxf(M, __ldcg(P.ws + recs.at(P, k) * record_floats(G) + G * kHeadDim + g));
+            float Ls = 0.f, Os = 0.f;
+            for (int k = 0; k < recs.count; ++k) {
+              const float* rec = P.ws + recs.at(P, k) * record_floats(G);
+              float f = fast_exp2(__ldcg(rec + G * kHeadDim + g) - M);
+              Ls = fmaf(__ldcg(rec + G * kHeadDim + 64 + g), f, Ls);
+              Os = fmaf(__ldcg(rec + g * kHeadDim + e), f, Os);
+            }
+            long long idx = (static_cast<long long>(pc.i) * P.Hq + pc.h * G + g) * kHeadDim + e;
+            store_out(P.out, idx, Ls > 0.f ? Os / Ls : 0.f, P.out_dtype);
+          }
+          if (tid == 0) *counter = 0;
+        }
+      }
+      // all consumers agree whether to stop; also guards the shared scratch
+      if (consumers_sync_or<NT>(ok ? 0 : 1)) break;
     }
   }
 
   // --- drain: never leave a bulk copy in flight into this CTA's memory ------
   __syncthreads();
   if (threadIdx.x == 0 && S.abort_flag) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       if (S.issued[s] > S.consumed[s]) {
         uint32_t parity = static_cast<uint32_t>((S.issued[s] - 1) & 1);
         long long t0 = global_ns();
@@ -683,97 +782,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params P) {
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge of partial records: one CTA (128 threads) per segment.
-//   M = max_p m_p;  out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p
-// Also writes the zero rows of empty sequences.
-// ---------------------------------------------------------------------------
-template <int G>
-__global__ void __launch_bounds__(128) merge_kernel(const Params P) {
-  const int i = blockIdx.x / P.Hkv;
-  const int h = blockIdx.x - i * P.Hkv;
-  const int e = threadIdx.x;
-  __shared__ long long red[2][4];
-  int L = P.seq_lens[i];
-  const int cap = P.max_blocks * kBlock;
-  L = L < 0 ? 0 : (L > cap ? cap : L);
-  const int nb = (L + kBlock - 1) / kBlock;
-  const long long row0 = (static_cast<long long>(i) * P.Hq + h * G) * kHeadDim;
-  if (nb == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) store_out(P.out, row0 + g * kHeadDim + e, 0.f, P.out_dtype);
-    return;
-  }
-  // prefix (sequences before i) and total of per-sequence counts
-  long long before = 0, total = 0;
-  for (int j = e; j < P.B; j += 128) {
-    int Lj = P.seq_lens[j];
-    Lj = Lj < 0 ? 0 : (Lj > cap ? cap : Lj);
-    int nbj = (Lj + kBlock - 1) / kBlock;
-    int c = P.sched == SCHED_LEAN ? nbj : (nbj + P.partition_blocks - 1) / P.partition_blocks;
-    total += c;
-    if (j < i) before += c;
-  }
-#pragma unroll
-  for (int msk = 16; msk >= 1; msk >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, msk);
-    total += __shfl_xor_sync(0xffffffffu, total, msk);
-  }
-  if ((e & 31) == 0) {
-    red[0][e >> 5] = before;
-    red[1][e >> 5] = total;
-  }
-  __syncthreads();
-  before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-  total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-
-  long long rec0, step = 0;
-  int count;
-  // LEAN: the records of the CTAs whose ranges cut this segment
-  long long c0 = 0, s0 = 0, per = 1;
-  if (P.sched == SCHED_LEAN) {
-    long long T = static_cast<long long>(P.Hkv) * total;
-    per = (T + P.lean_grid - 1) / P.lean_grid;
-    if (per < kLeanMinBlocks) per = kLeanMinBlocks;
-    s0 = static_cast<long long>(P.Hkv) * before + static_cast<long long>(h) * nb;
-    c0 = s0 / per;
-    long long c1 = (s0 + nb - 1) / per;
-    if (c0 == c1) return;  // written directly by the decode kernel
-    count = static_cast<int>(c1 - c0 + 1);
-    rec0 = 0;
-  } else {
-    int parts = (nb + P.partition_blocks - 1) / P.partition_blocks;
-    if (parts == 1) return;
-    count = parts;
-    rec0 = before * P.Hkv + h;
-    step = P.Hkv;
-  }
-  const int RF = record_floats(G);
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float M = -INFINITY;
-    for (int p = 0; p < count; ++p) {
-      long long r = P.sched == SCHED_LEAN
-                        ? 2 * (c0 + p) + ((p == 0 && s0 > c0 * per) ? 1 : 0)
-                        : rec0 + p * step;
-      M = fmaxf(M, P.ws[r * RF + G * kHeadDim + g]);
-    }
-    float Ls = 0.f, Os = 0.f;
-    for (int p = 0; p < count; ++p) {
-      long long r = P.sched == SCHED_LEAN
-                        ? 2 * (c0 + p) + ((p == 0 && s0 > c0 * per) ? 1 : 0)
-                        : rec0 + p * step;
-      const float* rec = P.ws + r * RF;
-      float f = fast_exp2(rec[G * kHeadDim + g] - M);
-      Ls = fmaf(rec[G * kHeadDim + 64 + g], f, Ls);
-      Os = fmaf(rec[g * kHeadDim + e], f, Os);
-    }
-    store_out(P.out, row0 + g * kHeadDim + e, Ls > 0.f ? Os / Ls : 0.f, P.out_dtype);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Host side: dispatch over (G, dtype, fused).
 // ---------------------------------------------------------------------------
+
 // Library-owned timing events (pa_profile_start / pa_profile_stop).
 static std::vector<cudaEvent_t> g_prof_events;  // [2 * capacity]
 static int g_prof_next = 0;
@@ -785,25 +796,26 @@ static void profile_release() {
 }
 
 template <int G, bool kBf16, bool kFused>
-static int occupancy_for(int B) {
+static int occupancy_for(size_t bytes) {
   static std::mutex mu;
-  static int cached_dev = -1, cached_B = -1, cached_occ = 0;
+  static int cached_dev = -1;
+  static size_t cached_bytes = 0;
+  static int cached_occ = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
-  if (dev == cached_dev && B == cached_B) return cached_occ;
-  size_t bytes = smem_bytes<G>(B);
+  if (dev == cached_dev && bytes == cached_bytes) return cached_occ;
   if (cudaFuncSetAttribute(decode_kernel<G, kBf16, kFused>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(bytes)) != cudaSuccess)
+                           static_cast<int>(smem_bytes<G>(kMaxSplitSeqs))) != cudaSuccess)
     return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G, kBf16, kFused>, kThreads,
-                                                    bytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G, kBf16, kFused>,
+                                                    Shape<G>::kThreads, bytes) != cudaSuccess)
     return 0;
   if (occ > kMaxCtasPerSm) occ = kMaxCtasPerSm;
   cached_dev = dev;
-  cached_B = B;
+  cached_bytes = bytes;
   cached_occ = occ;
   return occ;
 }
@@ -811,7 +823,8 @@ static int occupancy_for(int B) {
 template <int G, bool kBf16, bool kFused>
 static int launch_typed(Params& P, int device, cudaStream_t stream) {
   int B_smem = P.sched == SCHED_SEGMENT ? 0 : P.B;
-  int occ = occupancy_for<G, kBf16, kFused>(B_smem);
+  size_t bytes = smem_bytes<G>(B_smem);
+  int occ = occupancy_for<G, kBf16, kFused>(bytes);
   if (occ <= 0) return PA_ERR_CUDA;
   long long slots = static_cast<long long>(sm_count(device)) * occ;
   long long grid;
@@ -830,18 +843,12 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
   if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
   decode_kernel<G, kBf16, kFused>
-      <<<static_cast<int>(grid), kThreads, smem_bytes<G>(B_smem), stream>>>(P);
+      <<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
   if (timed) {
     if (cudaEventRecord(g_prof_events[2 * g_prof_next + 1], stream) != cudaSuccess) return PA_ERR_CUDA;
     ++g_prof_next;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (P.sched != SCHED_SEGMENT) {
-    merge_kernel<G><<<P.B * P.Hkv, 128, 0, stream>>>(P);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  }
-  return PA_OK;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 template <bool kBf16, bool kFused>
@@ -859,25 +866,29 @@ static int launch_g(int G, Params& P, int device, cudaStream_t stream) {
   }
 }
 
-static int choose_partition(int partition_blocks) {
-  return partition_blocks;  // 0 -> LEAN
-}
+// Workspace layout: partial records, then the per-segment counters at a
+// 256-byte aligned offset.
+struct WorkspaceLayout {
+  size_t records_bytes, counters_offset, total;
+};
 
-// Upper bound on the CTAs of a LEAN launch (for workspace sizing).
-static long long lean_grid_bound(int device) {
-  return static_cast<long long>(sm_count(device)) * kMaxCtasPerSm;
-}
-
-static size_t workspace_bytes_for(const pa_pool* p, int B, int Hq, int max_blocks, int partition_blocks) {
-  if (!p || B <= 0 || Hq <= 0 || max_blocks <= 0 || partition_blocks < 0) return 0;
-  if (Hq % p->n_kv_heads) return 0;
+static bool workspace_layout(const pa_pool* p, int B, int Hq, int max_blocks, int partition_blocks,
+                             WorkspaceLayout* out) {
+  if (!p || B <= 0 || Hq <= 0 || max_blocks <= 0 || partition_blocks < 0) return false;
+  if (Hq % p->n_kv_heads) return false;
   int G = Hq / p->n_kv_heads;
-  if (G > PA_MAX_GROUP) return 0;
+  if (G > PA_MAX_GROUP) return false;
   size_t rec = sizeof(float) * record_floats(G);
-  if (choose_partition(partition_blocks) == 0) return rec * 2 * lean_grid_bound(p->device);
-  size_t parts = static_cast<size_t>(B) * p->n_kv_heads *
-                 ((max_blocks + partition_blocks - 1) / partition_blocks);
-  return rec * parts;
+  size_t n_rec;
+  if (partition_blocks == 0)  // LEAN: two records per CTA of the largest grid
+    n_rec = 2 * static_cast<size_t>(sm_count(p->device)) * kMaxCtasPerSm;
+  else
+    n_rec = static_cast<size_t>(B) * p->n_kv_heads *
+            ((max_blocks + partition_blocks - 1) / partition_blocks);
+  out->records_bytes = rec * n_rec;
+  out->counters_offset = (out->records_bytes + 255) / 256 * 256;
+  out->total = out->counters_offset + sizeof(int) * static_cast<size_t>(B) * p->n_kv_heads;
+  return true;
 }
 
 static int decode_common(pa_pool_t p, const void* q, const void* k_new, const void* v_new,
@@ -894,12 +905,15 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   const bool fused = k_new != nullptr;
   if (fused && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15))
     return PA_ERR_INVALID;
+  WorkspaceLayout lay{};
   if (sched != SCHED_SEGMENT) {
     if (B > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
-    size_t need = workspace_bytes_for(p, B, Hq, max_blocks, partition_blocks);
-    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15)) return PA_ERR_INVALID;
+    if (!workspace_layout(p, B, Hq, max_blocks, partition_blocks, &lay)) return PA_ERR_INVALID;
+    if (!ws || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(ws) & 15)) return PA_ERR_INVALID;
   }
   Params P{};
+  P.tmap_k = p->tmap_k;
+  P.tmap_v = p->tmap_v;
   P.q = static_cast<const uint16_t*>(q);
   P.k_pool = static_cast<const uint16_t*>(p->k);
   P.v_pool = static_cast<const uint16_t*>(p->v);
@@ -909,6 +923,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.seq_lens = seq_lens;
   P.out = out;
   P.ws = static_cast<float*>(ws);
+  P.counters = ws ? reinterpret_cast<int*>(static_cast<char*>(ws) + lay.counters_offset) : nullptr;
   P.err = p->err;
   P.num_blocks = p->num_blocks;
   P.max_blocks = max_blocks;
@@ -971,7 +986,9 @@ int pa_decode(pa_pool_t p, const void* q, const int32_t* block_tables, int max_b
 
 size_t pa_decode_workspace_bytes(pa_pool_t p, int num_seqs, int n_q_heads, int max_blocks_per_seq,
                                  int partition_blocks) {
-  return workspace_bytes_for(p, num_seqs, n_q_heads, max_blocks_per_seq, partition_blocks);
+  WorkspaceLayout lay{};
+  if (!workspace_layout(p, num_seqs, n_q_heads, max_blocks_per_seq, partition_blocks, &lay)) return 0;
+  return lay.total;
 }
 
 int pa_decode_split(pa_pool_t p, const void* q, const int32_t* block_tables,

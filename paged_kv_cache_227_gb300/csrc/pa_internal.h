@@ -1,14 +1,20 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "pa.h"
 
 // One pool: K and V arrays [num_blocks][n_kv_heads][16][128] plus a device
-// error word.  Fixed-size physical blocks as in "Serving" 23.4.
+// error word.  Fixed-size physical blocks as in "Serving" 23.4.  Each array
+// also has a TMA tensor map that views it as a 2-D tensor of token rows
+// ([num_blocks*n_kv_heads*16][128]) and loads boxes of 16 rows x 64 elements
+// with the 128-byte swizzle, so one (block, head) tile is two boxes.
 struct pa_pool {
+  CUtensorMap tmap_k;  // CUtensorMap carries its own 64-byte alignment
+  CUtensorMap tmap_v;
   int num_blocks;
   int n_kv_heads;
   int dtype;          // PA_FP16 | PA_BF16

@@ -1,11 +1,45 @@
 // Pool lifetime, block copy for copy-on-write, the device error word and
 // status strings.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <vector>
 
 #include "pa_internal.h"
 
 namespace pa {
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point so
+// the library needs no link-time dependency on the driver library.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Token-row view of one pool array: dims {128, rows}, row stride 256 B, box
+// {64, 16} (128 B x 16 rows), 128-byte swizzle.
+static bool encode_pool_map(CUtensorMap* map, void* base, long long rows, int dtype) {
+  auto fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim / 2), static_cast<cuuint32_t>(kBlock)};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 int sm_count(int device) {
   static std::mutex mu;
@@ -71,6 +105,12 @@ int pa_pool_create(int num_blocks, int block_size, int n_kv_heads, int d_head, i
     cudaGetLastError();
     delete p;
     return PA_ERR_OOM;
+  }
+  const long long rows = static_cast<long long>(num_blocks) * n_kv_heads * kBlock;
+  if (!encode_pool_map(&p->tmap_k, p->k, rows, dtype) || !encode_pool_map(&p->tmap_v, p->v, rows, dtype)) {
+    cudaFree(p->k); cudaFree(p->v); cudaFree(p->err);
+    delete p;
+    return PA_ERR_CUDA;
   }
   if (cudaMemset(p->k, 0, p->bytes) != cudaSuccess || cudaMemset(p->v, 0, p->bytes) != cudaSuccess ||
       cudaMemset(p->err, 0, 2 * sizeof(long long)) != cudaSuccess ||
