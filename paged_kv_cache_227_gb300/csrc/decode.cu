@@ -33,14 +33,16 @@
 // tiles; the warps' states are merged at the end of each piece.
 //
 // Per tile a consumer warp runs two small tensor-core contractions with
-// mma.sync m16n8k16 (fp32 accumulate): the 16 MMA rows are the query heads
-// of the group (G <= 8, the rest zero), so
-//   S[g][t] = q_g . K[t]          2 n-tiles of 8 tokens x 8 k-steps of 16 dims
-//   O[g][:] += P[g][t] V[t][:]    16 n-tiles of 8 dims x 1 k-step of 16 tokens
-// The S accumulator fragments are exactly the A fragments of the second
-// product, so P never leaves registers.  P is split into a bf16/fp16 high
-// part and the rounded remainder, and both are multiplied, which keeps the
-// weights accurate to ~2^-17.  Softmax runs in fp32 in the log2 domain with
+// mma.sync m16n8k16 (fp32 accumulate) whose 8 columns are the query heads of
+// the group (G <= 8, the rest zero):
+//   S^T[t][g] = K[t] . q_g        M = 16 tokens, 8 k-steps of 16 dims
+//   O^T[:][g] += V^T P^T          8 m-tiles of 16 dims, k = 16 tokens
+// The score fragments are packed and transposed in registers (movmatrix) to
+// become the second product's B operand, so P never leaves registers.  P is
+// split into a 16-bit high part and the rounded remainder, and both are
+// multiplied, which keeps the weights accurate to ~2^-17.  That is 24 MMAs
+// per tile; the per-SM rate of this instruction is what bounds the kernel
+// once memory keeps up.  Softmax runs in fp32 in the log2 domain with
 // a lazily moved running max (rescale only when a new max exceeds the old by
 // 2^8).  Positions t >= L are masked by select on S and their V rows are
 // zeroed in shared memory, so padding or stale slots (even NaN) never reach
@@ -206,27 +208,27 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// D = A B + D for m16n8k16 with rows 8..15 of A zero: only the accumulator
-// of row group (lane / 4) is kept (d0, d1); a0/a2 are the row's k 0-7 / 8-15
-// pairs, b0/b1 the column's k 0-7 / 8-15 pairs.
+// D = A B + D for m16n8k16 (fp32 accumulate), all four A and C registers.
 template <bool kBf16>
-__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
-                                          uint32_t b1) {
-  float j0, j1;
-  const uint32_t z = 0;
-  const float fz = 0.f;
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   if (kBf16)
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(d0), "=f"(d1), "=f"(j0), "=f"(j1)
-        : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(fz), "f"(fz));
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   else
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(d0), "=f"(d1), "=f"(j0), "=f"(j1)
-        : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(fz), "f"(fz));
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Transpose of an 8x8 matrix of 16-bit elements held one row-pair per lane
+// (row lane/4, columns 2*(lane%4), +1): the result uses the same layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 // Two floats -> packed 16-bit pair (x in the low half), and the rounding
 // remainders of the pair as a second packed pair.
@@ -542,13 +544,19 @@ __global__ void __launch_bounds__(Shape<G>::kThreads)
     }
   } else {
     // ======================= consumer warps ================================
-    const int gq = lane >> 2;  // MMA row group = query head of the group this lane holds
-    const int tq = lane & 3;   // thread in the row group
+    // MMA fragment coordinates: row group r4 = lane / 4, column pair c4 = lane % 4.
+    //   scores  S^T[t][g]: rows t = r4, r4+8 (tokens), columns g = 2*c4, 2*c4+1
+    //   output  O^T[d][g]: rows d = 16*mt + r4, +8, the same columns g
+    const int r4 = lane >> 2;
+    const int c4 = lane & 3;
+    const int g0 = 2 * c4;       // first of this lane's two query heads
     const int tid = threadIdx.x;
-    // ldmatrix row addresses: lane group lm supplies matrix lm, row lr
+    // ldmatrix row addresses: lane group lm supplies matrix lm, row lr.  Both
+    // operands read [tok 0-7, chunk c], [tok 0-7, chunk c+1]... in the order
+    // (tok 0-7, c), (tok 8-15, c) for K and (tok 0-7, c), (tok 0-7, c+1) for V.
     const int lm = lane >> 3, lr = lane & 7;
-    const int k_tok = lr + 8 * (lm >> 1), k_cadd = lm & 1;  // K: [tok 0-7 | 8-15] x [chunk +0 | +1]
-    const int v_tok = lr + 8 * (lm & 1), v_cadd = lm >> 1;  // V: [tok 0-7 | 8-15] per chunk, transposed
+    const int k_tok = lr + 8 * (lm & 1), k_cadd = lm >> 1;  // A = K tile rows (tokens)
+    const int v_tok = lr + 8 * (lm >> 1), v_cadd = lm & 1;  // A = V^T via transposed loads
 
     // zero rows of empty sequences (split schedules; SEGMENT pieces write them)
     if (P.sched != SCHED_SEGMENT) {
@@ -567,24 +575,24 @@ __global__ void __launch_bounds__(Shape<G>::kThreads)
       const long long n0 = n;
       const int nblk = pc.j1 - pc.j0;
       n += nblk;
-      // A fragments of the query group (row gq; rows >= G are zero)
-      uint32_t qa[8][2];
-      if (gq < G) {
+      // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
+      uint32_t qb[8][2];
+      if (r4 < G) {
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + gq) * kHeadDim);
+            P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + r4) * kHeadDim);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          qa[ks][0] = qrow[8 * ks + tq];
-          qa[ks][1] = qrow[8 * ks + 4 + tq];
+          qb[ks][0] = qrow[8 * ks + c4];
+          qb[ks][1] = qrow[8 * ks + 4 + c4];
         }
       } else {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) qa[ks][0] = qa[ks][1] = 0u;
+        for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
       }
-      float o[16][2];
+      float o[8][4];
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = 0.f;
-      float m_run = -INFINITY, l_run = 0.f;
+      for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
       const int nb_total = (pc.L + kBlock - 1) / kBlock;
 
       // first tile of this warp in the piece
@@ -631,58 +639,60 @@ __global__ void __launch_bounds__(Shape<G>::kThreads)
             touched = true;
           }
           if (touched) __syncwarp();
-          // ---- S = Q K^T: 2 n-tiles (tokens 0-7, 8-15) x 8 k-steps
-          float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+          // ---- S^T = K Q^T: M = 16 tokens, N = 8 heads, 8 k-steps of 16 dims
+          float st[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            uint32_t b00, b01, b10, b11;
-            ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), b00, b01, b10, b11);
-            mma_rows8<kBf16>(sc[0][0], sc[0][1], qa[ks][0], qa[ks][1], b00, b01);
-            mma_rows8<kBf16>(sc[1][0], sc[1][1], qa[ks][0], qa[ks][1], b10, b11);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), a0, a1, a2, a3);
+            mma16816<kBf16>(st, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
           }
-          // ---- online softmax of row gq over tokens 2tq, 2tq+1, 8+2tq, 9+2tq
-          float mx = -INFINITY;
+          // ---- online softmax of columns g0, g0+1 over tokens r4, r4+8
+          float mx[2];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int c = 0; c < 2; ++c) {
+            st[c] = r4 < valid_tokens ? st[c] * P.qscale : -INFINITY;
+            st[2 + c] = r4 + 8 < valid_tokens ? st[2 + c] * P.qscale : -INFINITY;
+            mx[c] = fmaxf(st[c], st[2 + c]);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int t = 8 * nt + 2 * tq + c;
-              sc[nt][c] = t < valid_tokens ? sc[nt][c] * P.qscale : -INFINITY;
-              mx = fmaxf(mx, sc[nt][c]);
-            }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          if (mx > m_run + kRescaleThreshold) {  // uniform within the row group
-            const float mn = fmaxf(m_run, mx);
-            const float alpha = fast_exp2(m_run - mn);
-            l_run *= alpha;
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-              o[nt][0] *= alpha;
-              o[nt][1] *= alpha;
-            }
-            m_run = mn;
+            for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
           }
-          float p[2][2];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int c = 0; c < 2; ++c) {
+            if (mx[c] > m_run[c] + kRescaleThreshold) {  // uniform across the column's lanes
+              const float mn = fmaxf(m_run[c], mx[c]);
+              const float alpha = fast_exp2(m_run[c] - mn);
+              l_run[c] *= alpha;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              p[nt][c] = fast_exp2(sc[nt][c] - m_run);
-              l_run += p[nt][c];
+              for (int mt = 0; mt < 8; ++mt) {
+                o[mt][c] *= alpha;
+                o[mt][2 + c] *= alpha;
+              }
+              m_run[c] = mn;
             }
-          uint32_t ph0, pl0, ph1, pl1;  // A fragments of P: tokens 0-7 | 8-15, high and low parts
-          split_pack<kBf16>(p[0][0], p[0][1], ph0, pl0);
-          split_pack<kBf16>(p[1][0], p[1][1], ph1, pl1);
-          // ---- O += P V: 16 n-tiles of 8 dims, k = 16 tokens
+          }
+          float p[4];
 #pragma unroll
-          for (int pp = 0; pp < 8; ++pp) {
-            uint32_t b0a, b1a, b0b, b1b;
-            ldsm_x4_trans(vs_addr + swz(v_tok, 2 * pp + v_cadd), b0a, b1a, b0b, b1b);
-            mma_rows8<kBf16>(o[2 * pp][0], o[2 * pp][1], ph0, ph1, b0a, b1a);
-            mma_rows8<kBf16>(o[2 * pp][0], o[2 * pp][1], pl0, pl1, b0a, b1a);
-            mma_rows8<kBf16>(o[2 * pp + 1][0], o[2 * pp + 1][1], ph0, ph1, b0b, b1b);
-            mma_rows8<kBf16>(o[2 * pp + 1][0], o[2 * pp + 1][1], pl0, pl1, b0b, b1b);
+          for (int k = 0; k < 4; ++k) {
+            p[k] = fast_exp2(st[k] - m_run[k & 1]);
+            l_run[k & 1] += p[k];
+          }
+          // B fragments of P^T (k = tokens, n = heads): transpose the packed
+          // 8x8 blocks (tokens 0-7 and 8-15) of the score fragment
+          uint32_t h0, l0, h1, l1;
+          split_pack<kBf16>(p[0], p[1], h0, l0);
+          split_pack<kBf16>(p[2], p[3], h1, l1);
+          h0 = movmatrix_t(h0);
+          l0 = movmatrix_t(l0);
+          h1 = movmatrix_t(h1);
+          l1 = movmatrix_t(l1);
+          // ---- O^T += V^T P^T: M = 16 dims per m-tile (8 m-tiles), N = 8 heads, K = 16 tokens
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(vs_addr + swz(v_tok, 2 * mt + v_cadd), a0, a1, a2, a3);
+            mma16816<kBf16>(o[mt], a0, a1, a2, a3, h0, h1);
+            mma16816<kBf16>(o[mt], a0, a1, a2, a3, l0, l1);
           }
         }
         __syncwarp();
@@ -694,16 +704,25 @@ __global__ void __launch_bounds__(Shape<G>::kThreads)
       }
 
       // ---- merge the NW warps' states for this piece
-      float l = l_run;
-      l += __shfl_xor_sync(0xffffffffu, l, 1);
-      l += __shfl_xor_sync(0xffffffffu, l, 2);
-      if (gq < G) {
+      float lsum[2];
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-          *reinterpret_cast<float2*>(&S.ow[warp][gq][8 * nt + 2 * tq]) = make_float2(o[nt][0], o[nt][1]);
-        if (tq == 0) {
-          S.mw[warp][gq] = m_run;
-          S.lw[warp][gq] = l;
+      for (int c = 0; c < 2; ++c) {
+        lsum[c] = l_run[c];
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], msk);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (g0 + c < G) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            S.ow[warp][g0 + c][16 * mt + r4] = o[mt][c];
+            S.ow[warp][g0 + c][16 * mt + r4 + 8] = o[mt][2 + c];
+          }
+          if (r4 == 0) {
+            S.mw[warp][g0 + c] = m_run[c];
+            S.lw[warp][g0 + c] = lsum[c];
+          }
         }
       }
       consumers_sync<NT>();
