@@ -6,47 +6,40 @@
 // for one token per sequence, so it is bound by HBM bandwidth ("Serving",
 // section 23.2 Prefill and Decode); the design reads every K/V byte exactly
 // once, keeps enough bytes in flight to saturate HBM3e, and keeps the SM's
-// instruction issue far below the memory time.
+// instruction issue and its synchronisation well below the memory time.
 //
 // Work decomposition.  A segment is one (sequence i, kv head h) pair: its
 // nb_i = ceil(L_i/16) tiles of 16 tokens x 128 dims (4 KiB each for K and
-// for V).  The whole grouped-query head group (G = Hq/Hkv query heads) of the
-// segment is handled by the same CTA, so a tile is fetched once and used by G
-// heads.  A CTA is persistent and processes a list of pieces (a contiguous
-// range of a segment's tiles) given by one of three schedules:
-//   SEGMENT    whole segments, strided over CTAs (no workspace);
+// for V).  A tile is fetched once and used by all G = Hq/Hkv query heads of
+// the group.  The unit of work is one WARP: every warp of the persistent grid
+// is an independent pipeline with its own list of pieces (a contiguous range
+// of one segment's tiles) given by one of three schedules:
+//   SEGMENT    whole segments, strided over warps (no workspace);
 //   LEAN       the concatenated tile stream of all segments cut into equal
-//              per-CTA ranges (even load for any length mix); a segment cut
+//              per-warp ranges (even load for any length mix); a segment cut
 //              by a range boundary leaves partial results;
 //   PARTITION  fixed partitions of `partition_blocks` tiles per segment.
 // A piece that does not cover its whole segment writes a partial record
-// (running max m, sum l, unnormalised o, fp32) and bumps the segment's
-// counter; the CTA that completes the count merges the records by
-// log-sum-exp and writes the output, then resets the counter to zero.
+// (running max m, sum l, unnormalised o, fp32) and counts itself done on the
+// segment's counter with an acquire-release atomic; the warp that completes
+// the count merges the records by log-sum-exp, writes the output and resets
+// the counter to zero.
 //
-// CTA layout: 4 consumer warps + 1 producer warp, two CTAs per SM.  The
-// producer walks the block table and streams each (block, head) K and V tile
-// into a shared-memory ring of S = 12 stages (8 for G > 4) with TMA tensor
-// loads (two 16-row x 128-byte boxes per tile, 128-byte swizzle), completion
-// tracked by mbarriers.  Tile n of the CTA's stream goes to stage n % S and
-// is consumed by warp n % 4, which runs the online softmax over its own
-// tiles; the warps' states are merged at the end of each piece.
-//
-// Per tile a consumer warp runs two small tensor-core contractions with
-// mma.sync m16n8k16 (fp32 accumulate) whose 8 columns are the query heads of
-// the group (G <= 8, the rest zero):
-//   S^T[t][g] = K[t] . q_g        M = 16 tokens, 8 k-steps of 16 dims
-//   O^T[:][g] += V^T P^T          8 m-tiles of 16 dims, k = 16 tokens
-// The score fragments are packed and transposed in registers (movmatrix) to
-// become the second product's B operand, so P never leaves registers.  P is
-// split into a 16-bit high part and the rounded remainder, and both are
-// multiplied, which keeps the weights accurate to ~2^-17.  That is 24 MMAs
-// per tile; the per-SM rate of this instruction is what bounds the kernel
-// once memory keeps up.  Softmax runs in fp32 in the log2 domain with
-// a lazily moved running max (rescale only when a new max exceeds the old by
-// 2^8).  Positions t >= L are masked by select on S and their V rows are
-// zeroed in shared memory, so padding or stale slots (even NaN) never reach
-// the output.  ldmatrix reads the swizzled tiles without bank conflicts.
+// Per warp: a private ring of S shared-memory stages.  The warp streams its
+// tiles in with TMA tensor loads (two 16-row x 128-byte boxes per K or V
+// tile, 128-byte swizzle; completion on an mbarrier) and refills a stage the
+// moment it has finished with it, so S-1 tiles are always in flight and no
+// warp ever waits on another.  Per tile:
+//   scores  S^T[t][g] = K[t] . q_g with mma.sync m16n8k16 (M = 16 tokens,
+//           N = 8 query heads of the group, 8 k-steps of 16 dims, fp32
+//           accumulate, 4 independent accumulators); ldmatrix reads the
+//           swizzled K tile without bank conflicts;
+//   online softmax in fp32 in the log2 domain with a lazily moved running
+//           max (rescale only when a new max exceeds the old by 2^8);
+//   values  o[g][:] += p[t][g] V[t][:] in fp32 on the FMA pipes (packed
+//           two-wide FMAs), with p exact in fp32 (no rounding of weights).
+// Positions t >= L are masked by select in the scores and skipped in the
+// values, so padding or stale slots (even NaN) never reach the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -60,21 +53,20 @@ namespace pa {
 
 constexpr int kMaxSplitSeqs = 4096;  // sequences per split launch (prefix in shared memory)
 constexpr int kMaxCtasPerSm = 4;
-constexpr int kLeanMinBlocks = 8;    // smallest LEAN range per CTA
+constexpr int kLeanMinBlocks = 4;    // smallest LEAN range per warp
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 
 enum { SCHED_SEGMENT = 0, SCHED_LEAN = 1, SCHED_PARTITION = 2 };
 
-// Compile-time shape of the kernel: 4 consumer warps; 12 ring stages for
-// G <= 4 and 8 for larger groups (whose merge buffer is bigger), so that two
-// CTAs fit in an SM's shared memory either way.
+// Compile-time shape of the kernel: NW warps per CTA, SW ring stages per warp.
 template <int G>
 struct Shape {
-  static constexpr int NW = 4;                          // consumer warps (+1 producer)
-  static constexpr int kStages = G <= 4 ? 3 * NW : 2 * NW;
-  static constexpr int kThreads = (NW + 1) * 32;
+  static constexpr int NW = 4;
+  static constexpr int SW = 3;
+  static constexpr int kThreads = NW * 32;
+  static constexpr int PB = G <= 4 ? 4 : 8;  // row stride of the per-warp p buffer
 };
 
 struct Params {
@@ -98,7 +90,7 @@ struct Params {
   float qscale;             // scale * log2(e)
   int sched;
   int partition_blocks;     // PARTITION: tiles per partition
-  int lean_grid;            // LEAN: number of CTAs the ranges are cut for
+  int lean_units;           // LEAN: number of warps the ranges are cut for
   long long wait_limit_ns;
 };
 
@@ -107,7 +99,7 @@ struct Params {
 __host__ __device__ constexpr int record_floats(int G) { return (G + 1) * 128; }
 
 // ---------------------------------------------------------------------------
-// PTX helpers: mbarrier, bulk copy, timer, named barriers.
+// PTX helpers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -133,40 +125,58 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ long long global_ns() {
   long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-template <int NT>
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-}
-template <int NT>
-__device__ __forceinline__ int consumers_sync_or(int pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 2, %2, p;\n\t"
-      "selp.s32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(pred), "n"(NT)
-      : "memory");
-  return r;
-}
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// TMA tensor load of one box (x = element column, y = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A B + D for m16n8k16 (fp32 accumulate).
+template <bool kBf16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if (kBf16)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Acquire-release add at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+// Byte offset of 16-byte chunk c (0..15) of row r in a tile stored as two
+// 128-byte-swizzled boxes [16 rows][64 elements] (the TMA 128-byte swizzle
+// XORs the chunk index with the row index modulo 8 inside each 1024-byte
+// span).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
@@ -186,72 +196,19 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-
-// TMA tensor load of one box (x = element column, y = row) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-// D = A B + D for m16n8k16 (fp32 accumulate), all four A and C registers.
+// 16-bit -> fp32 pairs for 8 packed elements (element 2k in .x, 2k+1 in .y).
 template <bool kBf16>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  if (kBf16)
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  else
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// Transpose of an 8x8 matrix of 16-bit elements held one row-pair per lane
-// (row lane/4, columns 2*(lane%4), +1): the result uses the same layout.
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-// Two floats -> packed 16-bit pair (x in the low half), and the rounding
-// remainders of the pair as a second packed pair.
-template <bool kBf16>
-__device__ __forceinline__ void split_pack(float x, float y, uint32_t& hi, uint32_t& lo) {
-  if (kBf16) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-    float2 hf = __bfloat1622float2(h);
-    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<uint32_t*>(&h);
-    lo = *reinterpret_cast<uint32_t*>(&l);
-  } else {
-    __half2 h = __floats2half2_rn(x, y);
-    float2 hf = __half22float2(h);
-    __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<uint32_t*>(&h);
-    lo = *reinterpret_cast<uint32_t*>(&l);
+__device__ __forceinline__ void unpack8(const uint4& v, float2 f[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (kBf16) {
+      f[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+    } else {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
+      f[k] = __half22float2(h);
+    }
   }
-}
-// Byte offset of 16-byte chunk c (0..15) of row r in a tile stored as two
-// 128-byte-swizzled boxes [16 rows][64 elements].
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ void store_out(void* out, long long idx, float x, int out_dtype) {
@@ -261,6 +218,28 @@ __device__ __forceinline__ void store_out(void* out, long long idx, float x, int
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(x);
   else
     static_cast<__half*>(out)[idx] = __float2half_rn(x);
+}
+
+// Eight consecutive outputs starting at an index that is a multiple of 8.
+__device__ __forceinline__ void store_out8(void* out, long long idx, const float v[8], int out_dtype) {
+  if (out_dtype == PA_FP32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (out_dtype == PA_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t*>(&h);
+      } else {
+        __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + idx) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 __device__ __forceinline__ int clamp_len(const Params& P, int i) {
@@ -275,12 +254,13 @@ __device__ __forceinline__ int clamp_len(const Params& P, int i) {
 
 __device__ __forceinline__ long long lean_per(const Params& P, const int* pfx) {
   long long T = static_cast<long long>(P.Hkv) * pfx[P.B];
-  long long per = (T + P.lean_grid - 1) / P.lean_grid;
+  long long per = (T + P.lean_units - 1) / P.lean_units;
   return per < kLeanMinBlocks ? kLeanMinBlocks : per;
 }
 
 // ---------------------------------------------------------------------------
-// Piece enumeration: every thread of the CTA walks the same list.
+// Piece enumeration for one warp (unit u of n_units): the warp walks the
+// same list twice, once to issue its loads and once to consume them.
 // ---------------------------------------------------------------------------
 struct Piece {
   int i, h, j0, j1, L;
@@ -291,17 +271,19 @@ struct Piece {
 struct PieceIter {
   const Params& P;
   const int* pfx;  // shared: exclusive prefix over sequences (LEAN: tiles, PARTITION: partitions)
+  int unit, n_units;
   long long x, x_end;        // SEGMENT / PARTITION cursor
   long long cur, end;        // LEAN cursor
   int li, lh, lj;
   bool first;
 
-  __device__ PieceIter(const Params& p, const int* prefix) : P(p), pfx(prefix) {
+  __device__ PieceIter(const Params& p, const int* prefix, int u, int nu)
+      : P(p), pfx(prefix), unit(u), n_units(nu) {
     first = true;
     if (P.sched == SCHED_LEAN) {
       long long T = static_cast<long long>(P.Hkv) * pfx[P.B];
       long long per = lean_per(P, pfx);
-      cur = per * blockIdx.x;
+      cur = per * unit;
       end = cur + per < T ? cur + per : T;
       if (cur < end) {
         // largest i with Hkv*pfx[i] <= cur (never an empty sequence)
@@ -317,7 +299,7 @@ struct PieceIter {
         lj = static_cast<int>(off - static_cast<long long>(lh) * nb);
       }
     } else {
-      x = blockIdx.x;
+      x = unit;
       x_end = P.sched == SCHED_SEGMENT ? static_cast<long long>(P.B) * P.Hkv
                                        : static_cast<long long>(P.Hkv) * pfx[P.B];
     }
@@ -336,7 +318,7 @@ struct PieceIter {
       pc.j1 = lj + static_cast<int>(pend - cur);
       pc.L = clamp_len(P, li);
       pc.final_out = (lj == 0 && pend == seg_end);
-      pc.rec = 2ll * blockIdx.x + (first ? 0 : 1);
+      pc.rec = 2ll * unit + (first ? 0 : 1);
       first = false;
       cur = pend;
       if (cur == seg_end) {
@@ -376,7 +358,7 @@ struct PieceIter {
       pc.final_out = (pfx[lo + 1] - pfx[lo]) == 1;
       pc.rec = x;
     }
-    x += gridDim.x;
+    x += n_units;
     return true;
   }
 };
@@ -405,34 +387,26 @@ struct SegmentRecords {
   }
 };
 
-
 // ---------------------------------------------------------------------------
-// Shared memory.  The ring comes first at a 1024-byte aligned base (the
-// 128-byte swizzle of TMA boxes needs it); the mbarriers need 8 bytes.
+// Shared memory.  The rings come first at a 1024-byte aligned base (the
+// 128-byte swizzle of TMA boxes needs it); p buffers are 16-byte aligned.
 // ---------------------------------------------------------------------------
 template <int G>
 struct __align__(1024) Smem {
   static constexpr int NW = Shape<G>::NW;
-  static constexpr int S = Shape<G>::kStages;
-  uint8_t stage[S][kStageBytes];
-  __align__(16) float ow[NW][G][kHeadDim];
-  __align__(8) unsigned long long full[S];
-  unsigned long long empty[S];
-  float mw[NW][G];
-  float lw[NW][G];
-  int stage_blk[S];
-  int issued[S];
-  int consumed[S];
+  static constexpr int SW = Shape<G>::SW;
+  uint8_t stage[NW][SW][kStageBytes];
+  __align__(16) float pbuf[NW][kBlock][Shape<G>::PB];
+  __align__(8) unsigned long long full[NW][SW];
+  int stage_blk[NW][SW];
   int abort_flag;
-  int merge_flag;
   int pfx[1];  // [B + 1], dynamic tail
 };
 
 template <int G>
 constexpr bool smem_layout_ok() {
-  return offsetof(Smem<G>, stage) == 0 && offsetof(Smem<G>, ow) % 16 == 0 &&
-         offsetof(Smem<G>, full) % 8 == 0 && offsetof(Smem<G>, empty) % 8 == 0 &&
-         kStageBytes % 1024 == 0 && Shape<G>::kStages % Shape<G>::NW == 0;
+  return offsetof(Smem<G>, stage) == 0 && offsetof(Smem<G>, pbuf) % 16 == 0 &&
+         offsetof(Smem<G>, full) % 8 == 0 && kStageBytes % 1024 == 0;
 }
 static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() &&
                   smem_layout_ok<4>() && smem_layout_ok<5>() && smem_layout_ok<6>() &&
@@ -445,15 +419,15 @@ template <int G>
 constexpr size_t smem_bytes(int B) {
   return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>(B + 1) + 1024;
 }
+
 // ---------------------------------------------------------------------------
 // The decode kernel.
 // ---------------------------------------------------------------------------
 template <int G, bool kBf16, bool kFused>
-__global__ void __launch_bounds__(Shape<G>::kThreads)
-    decode_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid_constant__ Params P) {
   constexpr int NW = Shape<G>::NW;
-  constexpr int NS = Shape<G>::kStages;
-  constexpr int NT = NW * 32;  // consumer threads
+  constexpr int SW = Shape<G>::SW;
+  constexpr int PB = Shape<G>::PB;
   extern __shared__ uint8_t smem_raw[];
   Smem<G>& S = *reinterpret_cast<Smem<G>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -462,342 +436,387 @@ __global__ void __launch_bounds__(Shape<G>::kThreads)
 
   // --- set-up: barriers, prefix over sequences -----------------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_addr(&S.full[s]), 1);
-      mbar_init(smem_addr(&S.empty[s]), 1);
-      S.issued[s] = 0;
-      S.consumed[s] = 0;
-    }
+    for (int w = 0; w < NW; ++w)
+      for (int s = 0; s < SW; ++s) mbar_init(smem_addr(&S.full[w][s]), 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (P.sched != SCHED_SEGMENT && warp == 0) {
+  if (P.sched != SCHED_SEGMENT) {
     // exclusive prefix of per-sequence counts (tiles for LEAN, partitions for
-    // PARTITION), 32 sequences at a time
-    int carry = 0;
-    for (int base = 0; base < P.B; base += 32) {
-      int i = base + lane;
-      int c = 0;
-      if (i < P.B) {
-        int L = P.seq_lens[i];
-        int cap = P.max_blocks * kBlock;
-        L = L < 0 ? 0 : (L > cap ? cap : L);
-        int nb = (L + kBlock - 1) / kBlock;
-        c = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
-      }
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (i < P.B) S.pfx[i] = carry + incl - c;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+    // PARTITION): all threads fetch the counts, then warp 0 scans them
+    const int cap = P.max_blocks * kBlock;
+    for (int i = threadIdx.x; i < P.B; i += blockDim.x) {
+      int L = P.seq_lens[i];
+      L = L < 0 ? 0 : (L > cap ? cap : L);
+      int nb = (L + kBlock - 1) / kBlock;
+      S.pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
     }
-    if (lane == 0) S.pfx[P.B] = carry;
-  }
-  __syncthreads();
-
-  volatile int* abort_flag = &S.abort_flag;
-
-  if (warp == NW) {
-    // ======================= producer warp =================================
-    PieceIter it(P, S.pfx);
-    Piece pc;
-    long long n = 0;
-    bool ok = true;
-    while (ok && it.next(pc)) {
-      const int32_t* row = P.tables + static_cast<long long>(pc.i) * P.max_blocks;
-      for (int jb = pc.j0; ok && jb < pc.j1; jb += 32) {
-        int cnt = pc.j1 - jb < 32 ? pc.j1 - jb : 32;
-        int my_blk = lane < cnt ? row[jb + lane] : 0;
-        for (int k = 0; k < cnt; ++k, ++n) {
-          int blk = __shfl_sync(0xffffffffu, my_blk, k);
-          int s = static_cast<int>(n % NS);
-          if (lane == 0) {
-            if (n >= NS)
-              ok = wait_phase(smem_addr(&S.empty[s]), static_cast<uint32_t>(((n / NS) - 1) & 1),
-                              abort_flag, P.wait_limit_ns, P.err, 1);
-            if (ok) {
-              bool valid = blk >= 0 && blk < P.num_blocks;
-              S.stage_blk[s] = valid ? blk : -1;
-              S.issued[s] += 1;
-              uint32_t fb = smem_addr(&S.full[s]);
-              if (valid) {
-                mbar_arrive_expect_tx(fb, kStageBytes);
-                const int y = (blk * P.Hkv + pc.h) * kBlock;  // first token row of the tile
-                const uint32_t dst = smem_addr(S.stage[s]);
-                tma_load_2d(dst, &P.tmap_k, 0, y, fb);
-                tma_load_2d(dst + 2048, &P.tmap_k, kHeadDim / 2, y, fb);
-                tma_load_2d(dst + kTileBytes, &P.tmap_v, 0, y, fb);
-                tma_load_2d(dst + kTileBytes + 2048, &P.tmap_v, kHeadDim / 2, y, fb);
-              } else {
-                record_error(P.err, PA_ERR_DEVICE_CHECK, static_cast<long long>(blk));
-                mbar_arrive(fb);
-              }
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-        }
-      }
-    }
-  } else {
-    // ======================= consumer warps ================================
-    // MMA fragment coordinates: row group r4 = lane / 4, column pair c4 = lane % 4.
-    //   scores  S^T[t][g]: rows t = r4, r4+8 (tokens), columns g = 2*c4, 2*c4+1
-    //   output  O^T[d][g]: rows d = 16*mt + r4, +8, the same columns g
-    const int r4 = lane >> 2;
-    const int c4 = lane & 3;
-    const int g0 = 2 * c4;       // first of this lane's two query heads
-    const int tid = threadIdx.x;
-    // ldmatrix row addresses: lane group lm supplies matrix lm, row lr.  Both
-    // operands read [tok 0-7, chunk c], [tok 0-7, chunk c+1]... in the order
-    // (tok 0-7, c), (tok 8-15, c) for K and (tok 0-7, c), (tok 0-7, c+1) for V.
-    const int lm = lane >> 3, lr = lane & 7;
-    const int k_tok = lr + 8 * (lm & 1), k_cadd = lm >> 1;  // A = K tile rows (tokens)
-    const int v_tok = lr + 8 * (lm >> 1), v_cadd = lm & 1;  // A = V^T via transposed loads
-
-    // zero rows of empty sequences (split schedules; SEGMENT pieces write them)
-    if (P.sched != SCHED_SEGMENT) {
-      for (int i = blockIdx.x; i < P.B; i += gridDim.x) {
-        if (S.pfx[i + 1] != S.pfx[i]) continue;
-        for (int x = tid; x < P.Hq * kHeadDim; x += NT)
-          store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
-      }
-    }
-
-    PieceIter it(P, S.pfx);
-    Piece pc;
-    long long n = 0;  // tile counter of the CTA's stream
-    bool ok = true;
-    while (it.next(pc)) {
-      const long long n0 = n;
-      const int nblk = pc.j1 - pc.j0;
-      n += nblk;
-      // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
-      uint32_t qb[8][2];
-      if (r4 < G) {
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + r4) * kHeadDim);
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < P.B; base += 32) {
+        int i = base + lane;
+        int c = i < P.B ? S.pfx[i + 1] : 0;
+        int incl = c;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          qb[ks][0] = qrow[8 * ks + c4];
-          qb[ks][1] = qrow[8 * ks + 4 + c4];
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
-      }
-      float o[8][4];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-      const int nb_total = (pc.L + kBlock - 1) / kBlock;
-
-      // first tile of this warp in the piece
-      int first = static_cast<int>((warp - (n0 % NW) + NW) % NW);
-      for (int b = first; ok && b < nblk; b += NW) {
-        const long long nn = n0 + b;
-        const int s = static_cast<int>(nn % NS);
-        const uint32_t parity = static_cast<uint32_t>((nn / NS) & 1);
-        bool got = wait_phase(smem_addr(&S.full[s]), parity, abort_flag, P.wait_limit_ns, P.err, 2);
-        got = __all_sync(0xffffffffu, got);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        const int j = pc.j0 + b;
-        const int blk = S.stage_blk[s];
-        uint8_t* Ks = S.stage[s];
-        uint8_t* Vs = Ks + kTileBytes;
-        const uint32_t ks_addr = smem_addr(Ks), vs_addr = smem_addr(Vs);
-        const int valid_tokens = pc.L - j * kBlock < kBlock ? pc.L - j * kBlock : kBlock;
-        bool touched = false;
-        if (blk >= 0) {
-          if (kFused && j == nb_total - 1) {
-            // the new token: use the caller's k_new/v_new for position L-1
-            // and write it to its slot in the pool
-            const int tn = (pc.L - 1) & (kBlock - 1);
-            const int c = lane & 15;
-            const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
-            const long long dst =
-                ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
-            const uint16_t* from = (lane < 16 ? P.k_new : P.v_new) + src;
-            uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c);
-            *reinterpret_cast<uint4*>((lane < 16 ? Ks : Vs) + swz(tn, c)) = val;
-            uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
-            *reinterpret_cast<uint4*>(pool_w + dst + 8 * c) = val;
-            touched = true;
-          }
-          if (valid_tokens < kBlock) {
-            // V rows past the sequence end may hold anything (even NaN):
-            // zero them so that 0-weight rows contribute exactly 0
-            const int nz = (kBlock - valid_tokens) * 16;
-            for (int x = lane; x < nz; x += 32)
-              *reinterpret_cast<uint4*>(Vs + swz(valid_tokens + (x >> 4), x & 15)) = make_uint4(0, 0, 0, 0);
-            touched = true;
-          }
-          if (touched) __syncwarp();
-          // ---- S^T = K Q^T: M = 16 tokens, N = 8 heads, 8 k-steps of 16 dims
-          float st[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), a0, a1, a2, a3);
-            mma16816<kBf16>(st, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-          }
-          // ---- online softmax of columns g0, g0+1 over tokens r4, r4+8
-          float mx[2];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            st[c] = r4 < valid_tokens ? st[c] * P.qscale : -INFINITY;
-            st[2 + c] = r4 + 8 < valid_tokens ? st[2 + c] * P.qscale : -INFINITY;
-            mx[c] = fmaxf(st[c], st[2 + c]);
-#pragma unroll
-            for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
-          }
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            if (mx[c] > m_run[c] + kRescaleThreshold) {  // uniform across the column's lanes
-              const float mn = fmaxf(m_run[c], mx[c]);
-              const float alpha = fast_exp2(m_run[c] - mn);
-              l_run[c] *= alpha;
-#pragma unroll
-              for (int mt = 0; mt < 8; ++mt) {
-                o[mt][c] *= alpha;
-                o[mt][2 + c] *= alpha;
-              }
-              m_run[c] = mn;
-            }
-          }
-          float p[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            p[k] = fast_exp2(st[k] - m_run[k & 1]);
-            l_run[k & 1] += p[k];
-          }
-          // B fragments of P^T (k = tokens, n = heads): transpose the packed
-          // 8x8 blocks (tokens 0-7 and 8-15) of the score fragment
-          uint32_t h0, l0, h1, l1;
-          split_pack<kBf16>(p[0], p[1], h0, l0);
-          split_pack<kBf16>(p[2], p[3], h1, l1);
-          h0 = movmatrix_t(h0);
-          l0 = movmatrix_t(l0);
-          h1 = movmatrix_t(h1);
-          l1 = movmatrix_t(l1);
-          // ---- O^T += V^T P^T: M = 16 dims per m-tile (8 m-tiles), N = 8 heads, K = 16 tokens
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(vs_addr + swz(v_tok, 2 * mt + v_cadd), a0, a1, a2, a3);
-            mma16816<kBf16>(o[mt], a0, a1, a2, a3, h0, h1);
-            mma16816<kBf16>(o[mt], a0, a1, a2, a3, l0, l1);
-          }
+        for (int o = 1; o < 32; o <<= 1) {
+          int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
         __syncwarp();
-        if (touched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (lane == 0) {
-          S.consumed[s] += 1;
-          mbar_arrive(smem_addr(&S.empty[s]));
-        }
+        if (i < P.B) S.pfx[i + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
-
-      // ---- merge the NW warps' states for this piece
-      float lsum[2];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        lsum[c] = l_run[c];
-#pragma unroll
-        for (int msk = 4; msk < 32; msk <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], msk);
-      }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        if (g0 + c < G) {
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            S.ow[warp][g0 + c][16 * mt + r4] = o[mt][c];
-            S.ow[warp][g0 + c][16 * mt + r4 + 8] = o[mt][2 + c];
-          }
-          if (r4 == 0) {
-            S.mw[warp][g0 + c] = m_run[c];
-            S.lw[warp][g0 + c] = lsum[c];
-          }
-        }
-      }
-      consumers_sync<NT>();
-      for (int x = tid; x < G * kHeadDim; x += NT) {
-        const int g = x / kHeadDim, e = x % kHeadDim;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, S.mw[w][g]);
-        float Ls = 0.f, Os = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            float f = fast_exp2(S.mw[w][g] - M);
-            Ls = fmaf(S.lw[w][g], f, Ls);
-            Os = fmaf(S.ow[w][g][e], f, Os);
-          }
-        }
-        if (pc.final_out) {
-          long long idx = (static_cast<long long>(pc.i) * P.Hq + pc.h * G + g) * kHeadDim + e;
-          store_out(P.out, idx, Ls > 0.f ? Os / Ls : 0.f, P.out_dtype);
-        } else {
-          float* rec = P.ws + pc.rec * record_floats(G);
-          rec[g * kHeadDim + e] = Os;
-          if (e == 0) {
-            rec[G * kHeadDim + g] = M;
-            rec[G * kHeadDim + 64 + g] = Ls;
-          }
-        }
-      }
-      if (!pc.final_out) {
-        // ---- log-sum-exp merge by the CTA that completes the segment:
-        //   M = max_p m_p;  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p
-        __threadfence();
-        consumers_sync<NT>();
-        const SegmentRecords recs(P, S.pfx, pc.i, pc.h);
-        int* counter = P.counters + static_cast<long long>(pc.i) * P.Hkv + pc.h;
-        if (tid == 0) S.merge_flag = atomicAdd(counter, 1) == recs.count - 1;
-        consumers_sync<NT>();
-        if (S.merge_flag) {
-          __threadfence();
-          for (int x = tid; x < G * kHeadDim; x += NT) {
-            const int g = x / kHeadDim, e = x % kHeadDim;
-            float M = -INFINITY;
-            for (int k = 0; k < recs.count; ++k)
-              M = fmaxf(M, __ldcg(P.ws + recs.at(P, k) * record_floats(G) + G * kHeadDim + g));
-            float Ls = 0.f, Os = 0.f;
-            for (int k = 0; k < recs.count; ++k) {
-              const float* rec = P.ws + recs.at(P, k) * record_floats(G);
-              float f = fast_exp2(__ldcg(rec + G * kHeadDim + g) - M);
-              Ls = fmaf(__ldcg(rec + G * kHeadDim + 64 + g), f, Ls);
-              Os = fmaf(__ldcg(rec + g * kHeadDim + e), f, Os);
-            }
-            long long idx = (static_cast<long long>(pc.i) * P.Hq + pc.h * G + g) * kHeadDim + e;
-            store_out(P.out, idx, Ls > 0.f ? Os / Ls : 0.f, P.out_dtype);
-          }
-          if (tid == 0) *counter = 0;
-        }
-      }
-      // all consumers agree whether to stop; also guards the shared scratch
-      if (consumers_sync_or<NT>(ok ? 0 : 1)) break;
+      if (lane == 0) S.pfx[0] = 0;
     }
   }
-
-  // --- drain: never leave a bulk copy in flight into this CTA's memory ------
   __syncthreads();
-  if (threadIdx.x == 0 && S.abort_flag) {
-    for (int s = 0; s < NS; ++s) {
-      if (S.issued[s] > S.consumed[s]) {
-        uint32_t parity = static_cast<uint32_t>((S.issued[s] - 1) & 1);
-        long long t0 = global_ns();
-        while (!mbar_try_wait(smem_addr(&S.full[s]), parity) && global_ns() - t0 < P.wait_limit_ns) {
+
+  // zero rows of empty sequences (split schedules; SEGMENT pieces write them)
+  if (P.sched != SCHED_SEGMENT) {
+    for (int i = blockIdx.x; i < P.B; i += gridDim.x) {
+      if (S.pfx[i + 1] != S.pfx[i]) continue;
+      for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x)
+        store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
+    }
+  }
+
+  volatile int* abort_flag = &S.abort_flag;
+  const int unit = blockIdx.x * NW + warp;
+  const int n_units = gridDim.x * NW;
+  uint8_t* ring = S.stage[warp][0];
+  const uint32_t ring_addr = smem_addr(ring);
+  const uint32_t full0 = smem_addr(&S.full[warp][0]);
+
+  // MMA fragment coordinates: row group r4 = lane / 4, column pair c4.
+  //   scores S^T[t][g]: rows t = r4, r4 + 8 (tokens), columns g = 2*c4, +1
+  const int r4 = lane >> 2;
+  const int c4 = lane & 3;
+  const int g0 = 2 * c4;
+  // ldmatrix: lane group lm supplies matrix lm, row lr: [tok 0-7 | 8-15] x [chunk +0 | +1]
+  const int lm = lane >> 3, lr = lane & 7;
+  const int k_tok = lr + 8 * (lm & 1), k_cadd = lm >> 1;
+  // value phase: lane owns 16-byte chunk c16 of the V rows of token parity r16
+  const int c16 = lane & 15;
+  const int r16 = lane >> 4;
+
+  // ---- issue side: walks the piece list up to SW tiles ahead ---------------
+  PieceIter iss(P, S.pfx, unit, n_units);
+  Piece ip;
+  bool ihave = iss.next(ip);
+  int ij = ihave ? ip.j0 : 0;
+  bool tb_ok = false;
+  int tb_base = 0, tb_val = 0;
+  int n_issued = 0;
+  auto issue = [&](int stage) {
+    while (ihave && ij >= ip.j1) {
+      ihave = iss.next(ip);
+      if (ihave) {
+        ij = ip.j0;
+        tb_ok = false;
+      }
+    }
+    if (!ihave) return;
+    if (!tb_ok || ij - tb_base >= 32) {  // warp-uniform: refresh 32 table entries
+      tb_base = ij;
+      tb_ok = true;
+      const int jj = ij + lane;
+      tb_val = jj < ip.j1 ? P.tables[static_cast<long long>(ip.i) * P.max_blocks + jj] : 0;
+    }
+    const int blk = __shfl_sync(0xffffffffu, tb_val, ij - tb_base);
+    if (lane == 0) {
+      const bool valid = blk >= 0 && blk < P.num_blocks;
+      S.stage_blk[warp][stage] = valid ? blk : -1;
+      const uint32_t fb = full0 + 8 * stage;
+      if (valid) {
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        const int y = (blk * P.Hkv + ip.h) * kBlock;  // first token row of the tile
+        const uint32_t dst = ring_addr + stage * kStageBytes;
+        tma_load_2d(dst, &P.tmap_k, 0, y, fb);
+        tma_load_2d(dst + 2048, &P.tmap_k, kHeadDim / 2, y, fb);
+        tma_load_2d(dst + kTileBytes, &P.tmap_v, 0, y, fb);
+        tma_load_2d(dst + kTileBytes + 2048, &P.tmap_v, kHeadDim / 2, y, fb);
+      } else {
+        record_error(P.err, PA_ERR_DEVICE_CHECK, static_cast<long long>(blk));
+        mbar_arrive(fb);
+      }
+    }
+    ++ij;
+    ++n_issued;
+  };
+#pragma unroll 1
+  for (int s = 0; s < SW; ++s) issue(s);
+
+  // ---- consume side -----------------------------------------------------------
+  PieceIter cit(P, S.pfx, unit, n_units);
+  Piece pc;
+  int n = 0;  // tiles consumed by this warp
+  bool ok = true;
+  float (*pb)[PB] = S.pbuf[warp];
+  while (ok && cit.next(pc)) {
+    // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
+    uint32_t qb[8][2];
+    if (r4 < G) {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + r4) * kHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qb[ks][0] = qrow[8 * ks + c4];
+        qb[ks][1] = qrow[8 * ks + 4 + c4];
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+    }
+    float2 o[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const int nb_total = (pc.L + kBlock - 1) / kBlock;
+
+    for (int j = pc.j0; j < pc.j1; ++j, ++n) {
+      const int s = n % SW;
+      const uint32_t parity = static_cast<uint32_t>((n / SW) & 1);
+      bool got = wait_phase(full0 + 8 * s, parity, abort_flag, P.wait_limit_ns, P.err, 2);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      const int blk = S.stage_blk[warp][s];
+      uint8_t* Ks = ring + s * kStageBytes;
+      uint8_t* Vs = Ks + kTileBytes;
+      const uint32_t ks_addr = ring_addr + s * kStageBytes;
+      const int valid_tokens = pc.L - j * kBlock < kBlock ? pc.L - j * kBlock : kBlock;
+      bool touched = false;
+      if (blk >= 0) {
+        if (kFused && j == nb_total - 1) {
+          // the new token: use the caller's k_new/v_new for position L-1 and
+          // write it to its slot in the pool
+          const int tn = (pc.L - 1) & (kBlock - 1);
+          const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
+          const long long dst =
+              ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
+          const uint16_t* from = (lane < 16 ? P.k_new : P.v_new) + src;
+          uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c16);
+          *reinterpret_cast<uint4*>((lane < 16 ? Ks : Vs) + swz(tn, c16)) = val;
+          uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
+          *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = val;
+          touched = true;
+          __syncwarp();
         }
+        // ---- S^T = K Q^T in 4 independent accumulators
+        float acc[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), a0, a1, a2, a3);
+          mma16816<kBf16>(acc[ks & 3], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
+        float st[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st[c] = (acc[0][c] + acc[1][c]) + (acc[2][c] + acc[3][c]);
+        // ---- online softmax of columns g0, g0+1 over tokens r4, r4+8
+        float mx[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          st[c] = r4 < valid_tokens ? st[c] * P.qscale : -INFINITY;
+          st[2 + c] = r4 + 8 < valid_tokens ? st[2 + c] * P.qscale : -INFINITY;
+          mx[c] = fmaxf(st[c], st[2 + c]);
+#pragma unroll
+          for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
+        }
+        const bool grow = mx[0] > m_run[0] + kRescaleThreshold || mx[1] > m_run[1] + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {  // warp-uniform; rare after the first tile
+          float alpha[2];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const float mn = fmaxf(m_run[c], mx[c]);
+            alpha[c] = fast_exp2(m_run[c] - mn);
+            l_run[c] *= alpha[c];
+            m_run[c] = mn;
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float a = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              o[g][e].x *= a;
+              o[g][e].y *= a;
+            }
+          }
+        }
+        float p[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          p[k] = fast_exp2(st[k] - m_run[k & 1]);
+          l_run[k & 1] += p[k];
+        }
+        if (g0 < G) {
+          pb[r4][g0] = p[0];
+          pb[r4 + 8][g0] = p[2];
+        }
+        if (g0 + 1 < G) {
+          pb[r4][g0 + 1] = p[1];
+          pb[r4 + 8][g0 + 1] = p[3];
+        }
+        __syncwarp();
+        // ---- o += p V over this lane's tokens (parity r16) and dims (chunk c16)
+#pragma unroll
+        for (int k = 0; k < kBlock / 2; ++k) {
+          const int t = 2 * k + r16;
+          if (t < valid_tokens) {
+            uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz(t, c16));
+            float2 vf[4];
+            unpack8<kBf16>(raw, vf);
+            float pp[PB];
+#pragma unroll
+            for (int g4 = 0; g4 < PB; g4 += 4) {
+              float4 q4 = *reinterpret_cast<const float4*>(&pb[t][g4]);
+              pp[g4] = q4.x; pp[g4 + 1] = q4.y; pp[g4 + 2] = q4.z; pp[g4 + 3] = q4.w;
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float2 p2 = make_float2(pp[g], pp[g]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o[g][e] = __ffma2_rn(p2, vf[e], o[g][e]);
+            }
+          }
+        }
+      }
+      __syncwarp();  // every lane is done with the stage and with pb
+      if (touched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(s);      // refill the stage just freed
+    }
+    if (!ok) break;
+
+    // ---- finish the piece: combine the token parities, then output or record
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, 16);
+        o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, 16);
+      }
+    float lsum[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      lsum[c] = l_run[c];
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], msk);
+    }
+    float mg[G], lg[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      mg[g] = __shfl_sync(0xffffffffu, m_run[g & 1], g >> 1);
+      lg[g] = __shfl_sync(0xffffffffu, lsum[g & 1], g >> 1);
+    }
+    const long long row0 = (static_cast<long long>(pc.i) * P.Hq + pc.h * G) * kHeadDim;
+    if (pc.final_out) {
+      if (lane < 16) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float inv = lg[g] > 0.f ? 1.f / lg[g] : 0.f;
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[2 * e] = o[g][e].x * inv;
+            v[2 * e + 1] = o[g][e].y * inv;
+          }
+          store_out8(P.out, row0 + g * kHeadDim + 8 * c16, v, P.out_dtype);
+        }
+      }
+    } else {
+      float* rec = P.ws + pc.rec * record_floats(G);
+      if (lane < 16) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float4* dst = reinterpret_cast<float4*>(rec + g * kHeadDim + 8 * c16);
+          dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
+          dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          rec[G * kHeadDim + g] = mg[g];
+          rec[G * kHeadDim + 64 + g] = lg[g];
+        }
+      }
+      // ---- log-sum-exp merge by the warp that completes the segment:
+      //   M = max_p m_p;  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p
+      __syncwarp();
+      const SegmentRecords recs(P, S.pfx, pc.i, pc.h);
+      int* counter = P.counters + static_cast<long long>(pc.i) * P.Hkv + pc.h;
+      int last = 0;
+      if (lane == 0) last = atom_add_acq_rel(counter, 1) == recs.count - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        // one pass over the records with a running max; lane owns dims
+        // 4*lane .. 4*lane+3 of every head, so each record costs one 16-byte
+        // load per head and per lane, and unrolling keeps several records'
+        // loads in flight
+        __syncwarp();
+        float M[G], Ls[G];
+        float4 Os[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          M[g] = -INFINITY;
+          Ls[g] = 0.f;
+          Os[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 4
+        for (int k = 0; k < recs.count; ++k) {
+          const float* r = P.ws + recs.at(P, k) * record_floats(G);
+          float mk[G], lk[G];
+          float4 ok[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            mk[g] = __ldcg(r + G * kHeadDim + g);
+            lk[g] = __ldcg(r + G * kHeadDim + 64 + g);
+            ok[g] = __ldcg(reinterpret_cast<const float4*>(r + g * kHeadDim) + lane);
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float mn = fmaxf(M[g], mk[g]);
+            const float a = fast_exp2(M[g] - mn), b = fast_exp2(mk[g] - mn);
+            Ls[g] = fmaf(Ls[g], a, lk[g] * b);
+            Os[g].x = fmaf(Os[g].x, a, ok[g].x * b);
+            Os[g].y = fmaf(Os[g].y, a, ok[g].y * b);
+            Os[g].z = fmaf(Os[g].z, a, ok[g].z * b);
+            Os[g].w = fmaf(Os[g].w, a, ok[g].w * b);
+            M[g] = mn;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float inv = Ls[g] > 0.f ? 1.f / Ls[g] : 0.f;
+          const long long idx = row0 + g * kHeadDim + 4 * lane;
+          store_out(P.out, idx, Os[g].x * inv, P.out_dtype);
+          store_out(P.out, idx + 1, Os[g].y * inv, P.out_dtype);
+          store_out(P.out, idx + 2, Os[g].z * inv, P.out_dtype);
+          store_out(P.out, idx + 3, Os[g].w * inv, P.out_dtype);
+        }
+        if (lane == 0) *counter = 0;
       }
     }
   }
+
+  // --- drain: never leave a bulk copy in flight into this warp's ring -------
+  if (!ok && lane == 0) {
+    for (int k = n; k < n_issued; ++k) {
+      const uint32_t bar = full0 + 8 * (k % SW);
+      const uint32_t parity = static_cast<uint32_t>((k / SW) & 1);
+      const long long t0 = global_ns();
+      while (!mbar_try_wait(bar, parity) && global_ns() - t0 < P.wait_limit_ns) {
+      }
+    }
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -841,6 +860,7 @@ static int occupancy_for(size_t bytes) {
 
 template <int G, bool kBf16, bool kFused>
 static int launch_typed(Params& P, int device, cudaStream_t stream) {
+  constexpr int NW = Shape<G>::NW;
   int B_smem = P.sched == SCHED_SEGMENT ? 0 : P.B;
   size_t bytes = smem_bytes<G>(B_smem);
   int occ = occupancy_for<G, kBf16, kFused>(bytes);
@@ -849,20 +869,21 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   long long grid;
   if (P.sched == SCHED_SEGMENT) {
     long long segs = static_cast<long long>(P.B) * P.Hkv;
-    grid = segs < slots ? segs : slots;
+    long long need = (segs + NW - 1) / NW;
+    grid = need < slots ? need : slots;
   } else if (P.sched == SCHED_LEAN) {
     grid = slots;
-    P.lean_grid = static_cast<int>(grid);
   } else {
     long long parts = static_cast<long long>(P.B) * P.Hkv *
                       ((P.max_blocks + P.partition_blocks - 1) / P.partition_blocks);
-    grid = parts < slots ? parts : slots;
+    long long need = (parts + NW - 1) / NW;
+    grid = need < slots ? need : slots;
   }
   if (grid < 1) grid = 1;
+  P.lean_units = static_cast<int>(grid) * NW;
   const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
   if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
-  decode_kernel<G, kBf16, kFused>
-      <<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
+  decode_kernel<G, kBf16, kFused><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
   if (timed) {
     if (cudaEventRecord(g_prof_events[2 * g_prof_next + 1], stream) != cudaSuccess) return PA_ERR_CUDA;
     ++g_prof_next;
@@ -899,8 +920,8 @@ static bool workspace_layout(const pa_pool* p, int B, int Hq, int max_blocks, in
   if (G > PA_MAX_GROUP) return false;
   size_t rec = sizeof(float) * record_floats(G);
   size_t n_rec;
-  if (partition_blocks == 0)  // LEAN: two records per CTA of the largest grid
-    n_rec = 2 * static_cast<size_t>(sm_count(p->device)) * kMaxCtasPerSm;
+  if (partition_blocks == 0)  // LEAN: two records per warp of the largest grid
+    n_rec = 2 * static_cast<size_t>(sm_count(p->device)) * kMaxCtasPerSm * Shape<1>::NW;
   else
     n_rec = static_cast<size_t>(B) * p->n_kv_heads *
             ((max_blocks + partition_blocks - 1) / partition_blocks);
@@ -920,7 +941,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   if (Hq % p->n_kv_heads) return PA_ERR_INVALID;
   const int G = Hq / p->n_kv_heads;
   if (G > PA_MAX_GROUP) return PA_ERR_UNSUPPORTED;
-  if (reinterpret_cast<uintptr_t>(q) & 15) return PA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PA_ERR_INVALID;
   const bool fused = k_new != nullptr;
   if (fused && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15))
     return PA_ERR_INVALID;
@@ -953,7 +974,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.qscale = scale * kLog2e;
   P.sched = sched;
   P.partition_blocks = partition_blocks > 0 ? partition_blocks : 1;
-  P.lean_grid = 1;
+  P.lean_units = 1;
   P.wait_limit_ns = wait_limit_ns();
   cudaStream_t st = as_stream(stream);
   const bool bf16 = p->dtype == PA_BF16;
