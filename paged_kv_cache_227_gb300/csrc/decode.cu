@@ -26,8 +26,9 @@
 // the counter to zero.
 //
 // Per warp: a private ring of S shared-memory stages.  The warp streams its
-// tiles in with TMA tensor loads (two 16-row x 128-byte boxes per K or V
-// tile, 128-byte swizzle; completion on an mbarrier) and refills a stage the
+// tiles in with TMA tensor loads (one 8 KiB box per tile: the K and the V
+// tile, each as two 16-row x 128-byte swizzled halves; completion on an
+// mbarrier) and refills a stage the
 // moment it has finished with it, so S-1 tiles are always in flight and no
 // warp ever waits on another.  Per tile:
 //   scores  S^T[t][g] = K[t] . q_g with mma.sync m16n8k16 (M = 16 tokens,
@@ -63,15 +64,15 @@ enum { SCHED_SEGMENT = 0, SCHED_LEAN = 1, SCHED_PARTITION = 2 };
 // Compile-time shape of the kernel: NW warps per CTA, SW ring stages per warp.
 template <int G>
 struct Shape {
-  static constexpr int NW = 4;
+  static constexpr int NW = 2;
   static constexpr int SW = 3;
+  static constexpr int kMinCtas = 4;  // CTAs per SM the register budget is sized for
   static constexpr int kThreads = NW * 32;
   static constexpr int PB = G <= 4 ? 4 : 8;  // row stride of the per-warp p buffer
 };
 
 struct Params {
-  CUtensorMap tmap_k;       // token-row views of the pools (see pa_pool)
-  CUtensorMap tmap_v;
+  CUtensorMap tmap_kv;      // tile view of the K|V allocation (see pa_pool)
   const uint16_t* q;        // [B][Hq][128]
   const uint16_t* k_pool;   // [N][Hkv][16][128]
   const uint16_t* v_pool;
@@ -135,13 +136,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// TMA tensor load of one box (x = element column, y = row) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
+// TMA tensor load of the 4-D box at (0, y, 0, 0) into shared memory: one
+// (block, head) tile of K and of V.
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap* map, int y, uint32_t bar) {
+  const int z = 0;
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
           dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(z), "r"(y), "r"(z), "r"(z), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -424,7 +426,7 @@ constexpr size_t smem_bytes(int B) {
 // The decode kernel.
 // ---------------------------------------------------------------------------
 template <int G, bool kBf16, bool kFused>
-__global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode_kernel(const __grid_constant__ Params P) {
   constexpr int NW = Shape<G>::NW;
   constexpr int SW = Shape<G>::SW;
   constexpr int PB = Shape<G>::PB;
@@ -531,11 +533,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
       if (valid) {
         mbar_arrive_expect_tx(fb, kStageBytes);
         const int y = (blk * P.Hkv + ip.h) * kBlock;  // first token row of the tile
-        const uint32_t dst = ring_addr + stage * kStageBytes;
-        tma_load_2d(dst, &P.tmap_k, 0, y, fb);
-        tma_load_2d(dst + 2048, &P.tmap_k, kHeadDim / 2, y, fb);
-        tma_load_2d(dst + kTileBytes, &P.tmap_v, 0, y, fb);
-        tma_load_2d(dst + kTileBytes + 2048, &P.tmap_v, kHeadDim / 2, y, fb);
+        tma_load_tile(ring_addr + stage * kStageBytes, &P.tmap_kv, y, fb);
       } else {
         record_error(P.err, PA_ERR_DEVICE_CHECK, static_cast<long long>(blk));
         mbar_arrive(fb);
@@ -544,18 +542,13 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
     ++ij;
     ++n_issued;
   };
-#pragma unroll 1
-  for (int s = 0; s < SW; ++s) issue(s);
-
   // ---- consume side -----------------------------------------------------------
   PieceIter cit(P, S.pfx, unit, n_units);
   Piece pc;
-  int n = 0;  // tiles consumed by this warp
-  bool ok = true;
-  float (*pb)[PB] = S.pbuf[warp];
-  while (ok && cit.next(pc)) {
-    // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
-    uint32_t qb[8][2];
+  bool have_pc = cit.next(pc);
+  // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
+  uint32_t qb[8][2];
+  auto load_q = [&]() {
     if (r4 < G) {
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
           P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + r4) * kHeadDim);
@@ -568,6 +561,15 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
     }
+  };
+  if (have_pc) load_q();  // in flight while the first loads are issued
+#pragma unroll 1
+  for (int s = 0; s < SW; ++s) issue(s);
+
+  int n = 0;  // tiles consumed by this warp
+  bool ok = true;
+  float (*pb)[PB] = S.pbuf[warp];
+  while (ok && have_pc) {
     float2 o[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -576,47 +578,65 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     const int nb_total = (pc.L + kBlock - 1) / kBlock;
 
-    for (int j = pc.j0; j < pc.j1; ++j, ++n) {
-      const int s = n % SW;
-      const uint32_t parity = static_cast<uint32_t>((n / SW) & 1);
+    // ---- tile loop, software-pipelined: the score product of tile j+1 is
+    // issued before the value product of tile j, so tensor-core latency hides
+    // behind the FMA work.
+    // prepare(): wait for the tile's stage, read its block id, and for the
+    // fused append put the new token into the tile and the pool.
+    auto prepare = [&](int jj, int nn, int& blk_out, bool& touched_out) -> bool {
+      const int s = nn % SW;
+      const uint32_t parity = static_cast<uint32_t>((nn / SW) & 1);
       bool got = wait_phase(full0 + 8 * s, parity, abort_flag, P.wait_limit_ns, P.err, 2);
       got = __all_sync(0xffffffffu, got);
-      if (!got) {
-        ok = false;
-        break;
-      }
+      touched_out = false;
+      blk_out = -1;
+      if (!got) return false;
       const int blk = S.stage_blk[warp][s];
-      uint8_t* Ks = ring + s * kStageBytes;
-      uint8_t* Vs = Ks + kTileBytes;
+      blk_out = blk;
+      if (blk >= 0 && kFused && jj == nb_total - 1) {
+        // the new token: use the caller's k_new/v_new for position L-1 and
+        // write it to its slot in the pool
+        uint8_t* Ks = ring + s * kStageBytes;
+        const int tn = (pc.L - 1) & (kBlock - 1);
+        const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
+        const long long dst = ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
+        const uint16_t* from = (lane < 16 ? P.k_new : P.v_new) + src;
+        uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c16);
+        *reinterpret_cast<uint4*>((lane < 16 ? Ks : Ks + kTileBytes) + swz(tn, c16)) = val;
+        uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
+        *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = val;
+        touched_out = true;
+        __syncwarp();
+      }
+      return true;
+    };
+    // S^T = K Q^T for the tile in stage s, in 4 independent accumulators
+    auto scores = [&](int s, float (&acc)[4][4]) {
       const uint32_t ks_addr = ring_addr + s * kStageBytes;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), a0, a1, a2, a3);
+        mma16816<kBf16>(acc[ks & 3], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+    };
+
+    float acc[4][4];
+    int cur_blk = -1;
+    bool cur_touched = false;
+    if (pc.j1 > pc.j0) {
+      if (!prepare(pc.j0, n, cur_blk, cur_touched))
+        ok = false;
+      else if (cur_blk >= 0)
+        scores(n % SW, acc);
+    }
+    for (int j = pc.j0; ok && j < pc.j1; ++j) {
+      const int s = n % SW;
+      const uint8_t* Vs = ring + s * kStageBytes + kTileBytes;
       const int valid_tokens = pc.L - j * kBlock < kBlock ? pc.L - j * kBlock : kBlock;
-      bool touched = false;
-      if (blk >= 0) {
-        if (kFused && j == nb_total - 1) {
-          // the new token: use the caller's k_new/v_new for position L-1 and
-          // write it to its slot in the pool
-          const int tn = (pc.L - 1) & (kBlock - 1);
-          const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
-          const long long dst =
-              ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
-          const uint16_t* from = (lane < 16 ? P.k_new : P.v_new) + src;
-          uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c16);
-          *reinterpret_cast<uint4*>((lane < 16 ? Ks : Vs) + swz(tn, c16)) = val;
-          uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
-          *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = val;
-          touched = true;
-          __syncwarp();
-        }
-        // ---- S^T = K Q^T in 4 independent accumulators
-        float acc[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), a0, a1, a2, a3);
-          mma16816<kBf16>(acc[ks & 3], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-        }
+      if (cur_blk >= 0) {
         float st[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) st[c] = (acc[0][c] + acc[1][c]) + (acc[2][c] + acc[3][c]);
@@ -642,11 +662,11 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
           }
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            const float a = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
+            const float al = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              o[g][e].x *= a;
-              o[g][e].y *= a;
+              o[g][e].x *= al;
+              o[g][e].y *= al;
             }
           }
         }
@@ -665,32 +685,77 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
           pb[r4 + 8][g0 + 1] = p[3];
         }
         __syncwarp();
-        // ---- o += p V over this lane's tokens (parity r16) and dims (chunk c16)
+      }
+      // ---- next tile: wait for it and issue its score product now
+      int nxt_blk = -1;
+      bool nxt_touched = false;
+      float acc2[4][4];
+      if (j + 1 < pc.j1) {
+        if (!prepare(j + 1, n + 1, nxt_blk, nxt_touched))
+          ok = false;
+        else if (nxt_blk >= 0)
+          scores((n + 1) % SW, acc2);
+      }
+      // ---- o += p V over this lane's tokens (parity r16) and dims (chunk c16)
+      if (cur_blk >= 0) {
+        if (valid_tokens == kBlock) {  // full tile: no per-token branch, loads hoisted
+          uint4 raw[kBlock / 2];
+          float pp[kBlock / 2][PB];
 #pragma unroll
-        for (int k = 0; k < kBlock / 2; ++k) {
-          const int t = 2 * k + r16;
-          if (t < valid_tokens) {
-            uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz(t, c16));
-            float2 vf[4];
-            unpack8<kBf16>(raw, vf);
-            float pp[PB];
+          for (int k = 0; k < kBlock / 2; ++k) {
+            const int t = 2 * k + r16;
+            raw[k] = *reinterpret_cast<const uint4*>(Vs + swz(t, c16));
 #pragma unroll
             for (int g4 = 0; g4 < PB; g4 += 4) {
               float4 q4 = *reinterpret_cast<const float4*>(&pb[t][g4]);
-              pp[g4] = q4.x; pp[g4 + 1] = q4.y; pp[g4 + 2] = q4.z; pp[g4 + 3] = q4.w;
+              pp[k][g4] = q4.x; pp[k][g4 + 1] = q4.y; pp[k][g4 + 2] = q4.z; pp[k][g4 + 3] = q4.w;
             }
+          }
+#pragma unroll
+          for (int k = 0; k < kBlock / 2; ++k) {
+            float2 vf[4];
+            unpack8<kBf16>(raw[k], vf);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const float2 p2 = make_float2(pp[g], pp[g]);
+              const float2 p2 = make_float2(pp[k][g], pp[k][g]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) o[g][e] = __ffma2_rn(p2, vf[e], o[g][e]);
+            }
+          }
+        } else {  // the sequence's last tile: skip the rows past its end
+#pragma unroll
+          for (int k = 0; k < kBlock / 2; ++k) {
+            const int t = 2 * k + r16;
+            if (t < valid_tokens) {
+              uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz(t, c16));
+              float2 vf[4];
+              unpack8<kBf16>(raw, vf);
+              float pp[PB];
+#pragma unroll
+              for (int g4 = 0; g4 < PB; g4 += 4) {
+                float4 q4 = *reinterpret_cast<const float4*>(&pb[t][g4]);
+                pp[g4] = q4.x; pp[g4 + 1] = q4.y; pp[g4 + 2] = q4.z; pp[g4 + 3] = q4.w;
+              }
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                const float2 p2 = make_float2(pp[g], pp[g]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[g][e] = __ffma2_rn(p2, vf[e], o[g][e]);
+              }
             }
           }
         }
       }
       __syncwarp();  // every lane is done with the stage and with pb
-      if (touched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (cur_touched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(s);      // refill the stage just freed
+      ++n;
+      cur_blk = nxt_blk;
+      cur_touched = nxt_touched;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[c][e] = acc2[c][e];
     }
     if (!ok) break;
 
@@ -756,40 +821,58 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
       if (lane == 0) last = atom_add_acq_rel(counter, 1) == recs.count - 1;
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
-        // one pass over the records with a running max; lane owns dims
-        // 4*lane .. 4*lane+3 of every head, so each record costs one 16-byte
-        // load per head and per lane, and unrolling keeps several records'
-        // loads in flight
+        // merge: lane k fetches record k's m and l (one round trip for up to
+        // 32 records at a time); the warp forms M = max m and the weights
+        // 2^(m_k - M); then every lane accumulates its 4 dims of every head
+        // over the records, whose 16-byte loads are independent and unrolled
         __syncwarp();
-        float M[G], Ls[G];
+        float M[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) M[g] = -INFINITY;
+        for (int base = 0; base < recs.count; base += 32) {
+          const int k = base + lane;
+          const float* r = P.ws + (k < recs.count ? recs.at(P, k) : 0) * record_floats(G);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float mk = k < recs.count ? __ldcg(r + G * kHeadDim + g) : -INFINITY;
+#pragma unroll
+            for (int msk = 1; msk < 32; msk <<= 1) mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, msk));
+            M[g] = fmaxf(M[g], mk);
+          }
+        }
+        float Ls[G];
         float4 Os[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          M[g] = -INFINITY;
           Ls[g] = 0.f;
           Os[g] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-#pragma unroll 4
-        for (int k = 0; k < recs.count; ++k) {
-          const float* r = P.ws + recs.at(P, k) * record_floats(G);
-          float mk[G], lk[G];
-          float4 ok[G];
+        for (int base = 0; base < recs.count; base += 32) {
+          const int k = base + lane;
+          const bool have = k < recs.count;
+          const float* r = P.ws + (have ? recs.at(P, k) : 0) * record_floats(G);
+          float w[G];
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            mk[g] = __ldcg(r + G * kHeadDim + g);
-            lk[g] = __ldcg(r + G * kHeadDim + 64 + g);
-            ok[g] = __ldcg(reinterpret_cast<const float4*>(r + g * kHeadDim) + lane);
+            w[g] = have ? fast_exp2(__ldcg(r + G * kHeadDim + g) - M[g]) : 0.f;
+            float lw = have ? __ldcg(r + G * kHeadDim + 64 + g) * w[g] : 0.f;
+#pragma unroll
+            for (int msk = 1; msk < 32; msk <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, msk);
+            Ls[g] += lw;
           }
+          const int cnt = recs.count - base < 32 ? recs.count - base : 32;
+#pragma unroll 8
+          for (int kk = 0; kk < cnt; ++kk) {
+            const float* rk = P.ws + recs.at(P, base + kk) * record_floats(G);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float mn = fmaxf(M[g], mk[g]);
-            const float a = fast_exp2(M[g] - mn), b = fast_exp2(mk[g] - mn);
-            Ls[g] = fmaf(Ls[g], a, lk[g] * b);
-            Os[g].x = fmaf(Os[g].x, a, ok[g].x * b);
-            Os[g].y = fmaf(Os[g].y, a, ok[g].y * b);
-            Os[g].z = fmaf(Os[g].z, a, ok[g].z * b);
-            Os[g].w = fmaf(Os[g].w, a, ok[g].w * b);
-            M[g] = mn;
+            for (int g = 0; g < G; ++g) {
+              const float wk = __shfl_sync(0xffffffffu, w[g], kk);
+              const float4 ok = __ldcg(reinterpret_cast<const float4*>(rk + g * kHeadDim) + lane);
+              Os[g].x = fmaf(ok.x, wk, Os[g].x);
+              Os[g].y = fmaf(ok.y, wk, Os[g].y);
+              Os[g].z = fmaf(ok.z, wk, Os[g].z);
+              Os[g].w = fmaf(ok.w, wk, Os[g].w);
+            }
           }
         }
 #pragma unroll
@@ -804,6 +887,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads) decode_kernel(const __grid
         if (lane == 0) *counter = 0;
       }
     }
+    have_pc = cit.next(pc);
+    if (have_pc) load_q();
   }
 
   // --- drain: never leave a bulk copy in flight into this warp's ring -------
@@ -952,8 +1037,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
     if (!ws || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(ws) & 15)) return PA_ERR_INVALID;
   }
   Params P{};
-  P.tmap_k = p->tmap_k;
-  P.tmap_v = p->tmap_v;
+  P.tmap_kv = p->tmap_kv;
   P.q = static_cast<const uint16_t*>(q);
   P.k_pool = static_cast<const uint16_t*>(p->k);
   P.v_pool = static_cast<const uint16_t*>(p->v);

@@ -8,13 +8,13 @@
 #include "pa.h"
 
 // One pool: K and V arrays [num_blocks][n_kv_heads][16][128] plus a device
-// error word.  Fixed-size physical blocks as in "Serving" 23.4.  Each array
-// also has a TMA tensor map that views it as a 2-D tensor of token rows
-// ([num_blocks*n_kv_heads*16][128]) and loads boxes of 16 rows x 64 elements
-// with the 128-byte swizzle, so one (block, head) tile is two boxes.
+// error word.  Fixed-size physical blocks as in "Serving" 23.4.  K and V sit
+// in one allocation (V right after K) so that one TMA tensor map covers both:
+// it views the pair as a 4-D tensor {64 elements, token rows, 2 row halves,
+// K|V} and loads a whole (block, head) tile of K and of V - 16 rows x 128
+// elements each - as one box, with the 128-byte swizzle.
 struct pa_pool {
-  CUtensorMap tmap_k;  // CUtensorMap carries its own 64-byte alignment
-  CUtensorMap tmap_v;
+  CUtensorMap tmap_kv;  // CUtensorMap carries its own 64-byte alignment
   int num_blocks;
   int n_kv_heads;
   int dtype;          // PA_FP16 | PA_BF16

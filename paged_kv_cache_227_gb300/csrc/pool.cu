@@ -25,17 +25,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
-// Token-row view of one pool array: dims {128, rows}, row stride 256 B, box
-// {64, 16} (128 B x 16 rows), 128-byte swizzle.
-static bool encode_pool_map(CUtensorMap* map, void* base, long long rows, int dtype) {
+// Tile view of the K|V allocation: dims {64 elements, rows, 2 halves, K|V}
+// with byte strides {256 (row), 128 (half), bytes of one array}; the box
+// {64, 16, 2, 2} is one (block, head) tile of K followed by the same tile of
+// V, written to shared memory as [K|V][half][row][128 bytes] with the 128-byte
+// swizzle.
+static bool encode_pool_map(CUtensorMap* map, void* base, long long rows, size_t array_bytes,
+                            int dtype) {
   auto fn = encode_tiled();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim / 2), static_cast<cuuint32_t>(kBlock)};
-  cuuint32_t elem[2] = {1, 1};
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim / 2), static_cast<cuuint64_t>(rows), 2, 2};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kRowBytes), static_cast<cuuint64_t>(kRowBytes / 2),
+                           static_cast<cuuint64_t>(array_bytes)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kHeadDim / 2), static_cast<cuuint32_t>(kBlock), 2, 2};
+  cuuint32_t elem[4] = {1, 1, 1, 1};
   CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  4, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -99,23 +104,25 @@ int pa_pool_create(int num_blocks, int block_size, int n_kv_heads, int d_head, i
   p->dtype = dtype;
   p->bytes = pa_pool_bytes(num_blocks, block_size, n_kv_heads, d_head, dtype);
   if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return PA_ERR_CUDA; }
-  if (cudaMalloc(&p->k, p->bytes) != cudaSuccess || cudaMalloc(&p->v, p->bytes) != cudaSuccess ||
-      cudaMalloc(&p->err, 2 * sizeof(long long)) != cudaSuccess) {
-    cudaFree(p->k); cudaFree(p->v); cudaFree(p->err);
+  void* kv = nullptr;
+  if (cudaMalloc(&kv, 2 * p->bytes) != cudaSuccess || cudaMalloc(&p->err, 2 * sizeof(long long)) != cudaSuccess) {
+    cudaFree(kv); cudaFree(p->err);
     cudaGetLastError();
     delete p;
     return PA_ERR_OOM;
   }
+  p->k = kv;
+  p->v = static_cast<char*>(kv) + p->bytes;
   const long long rows = static_cast<long long>(num_blocks) * n_kv_heads * kBlock;
-  if (!encode_pool_map(&p->tmap_k, p->k, rows, dtype) || !encode_pool_map(&p->tmap_v, p->v, rows, dtype)) {
-    cudaFree(p->k); cudaFree(p->v); cudaFree(p->err);
+  if (!encode_pool_map(&p->tmap_kv, kv, rows, p->bytes, dtype)) {
+    cudaFree(kv); cudaFree(p->err);
     delete p;
     return PA_ERR_CUDA;
   }
-  if (cudaMemset(p->k, 0, p->bytes) != cudaSuccess || cudaMemset(p->v, 0, p->bytes) != cudaSuccess ||
+  if (cudaMemset(kv, 0, 2 * p->bytes) != cudaSuccess ||
       cudaMemset(p->err, 0, 2 * sizeof(long long)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
-    cudaFree(p->k); cudaFree(p->v); cudaFree(p->err);
+    cudaFree(kv); cudaFree(p->err);
     delete p;
     return PA_ERR_CUDA;
   }
@@ -129,8 +136,7 @@ int pa_pool_destroy(pa_pool_t p) {
   cudaGetDevice(&prev);
   cudaSetDevice(p->device);
   cudaDeviceSynchronize();
-  cudaFree(p->k);
-  cudaFree(p->v);
+  cudaFree(p->k);  // K and V share one allocation
   cudaFree(p->err);
   cudaSetDevice(prev);
   delete p;
