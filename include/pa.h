@@ -57,7 +57,8 @@ enum {
   PA_ERR_OOM = -3,          /* device allocation or allocator free list empty */
   PA_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed           */
   PA_ERR_DEVICE_CHECK = -5, /* a kernel met an out-of-range block id or slot  */
-  PA_ERR_TIMEOUT = -6       /* a bounded in-kernel wait ran out               */
+  PA_ERR_TIMEOUT = -6,      /* a bounded in-kernel wait ran out               */
+  PA_ERR_SCRATCH_LIMIT = -7 /* needs more than the library's static scratch   */
 };
 
 enum { PA_BLOCK_SIZE = 16, PA_HEAD_DIM = 128, PA_MAX_GROUP = 8 };
@@ -177,6 +178,35 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
                      int num_seqs, int n_q_heads, float scale, void* out,
                      int out_dtype, int partition_blocks, void* workspace,
                      size_t workspace_bytes, void* stream);
+
+/* Split-KV decode that allocates nothing (the pages have no counterpart; this
+ * is a deployment convenience).  Some callers cannot call cudaMalloc at the
+ * time they decode: a serving loop whose device memory budget is fixed up
+ * front, or a host that links this library without any allocator of its
+ * own.  This call is
+ * pa_decode_split with partition_blocks as there, but its workspace is a
+ * static device array owned by the library instead of a caller buffer.
+ *  - Limit: the array holds PA_STATIC_SCRATCH_BYTES (12 MiB); a call whose
+ *    pa_decode_workspace_bytes(...) exceeds it returns PA_ERR_SCRATCH_LIMIT
+ *    before launching anything.  With partition_blocks == 0 this fits every
+ *    group size up to 8 on a 152-SM GPU; fixed partitions fit while
+ *    num_seqs * n_kv_heads * ceil(max_blocks_per_seq / partition_blocks)
+ *    records (each (G+1)*512 bytes) stay under the limit.
+ *  - Every GPU that loads the library keeps the 12 MiB until the process
+ *    exits.  The first call on a device looks the array's device address up
+ *    (cudaGetSymbolAddress, with that device current) and caches it, so make
+ *    the first call on each device before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents; the
+ *    call clears the part that must start at zero (the per-pair counters)
+ *    with an asynchronous memset on `stream`.  Calls that overlap on the GPU
+ *    (two streams, or two devices' calls racing on one device's array) race
+ *    on the array: serialise them.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called. */
+enum { PA_STATIC_SCRATCH_BYTES = 12 << 20 };
+int pa_decode_split_static(pa_pool_t pool, const void* q, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* seq_lens,
+                           int num_seqs, int n_q_heads, float scale, void* out,
+                           int out_dtype, int partition_blocks, void* stream);
 
 /* Copy-on-write support: copies whole blocks (all kv heads, K and V) from
  * src[j] to dst[j], j < n, both device int32 arrays.  The destinations must be

@@ -19,6 +19,8 @@ PA_FP16, PA_BF16, PA_FP32 = 0, 1, 2
 PA_OK = 0
 PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM = -1, -2, -3
 PA_ERR_CUDA, PA_ERR_DEVICE_CHECK, PA_ERR_TIMEOUT = -4, -5, -6
+PA_ERR_SCRATCH_LIMIT = -7
+PA_STATIC_SCRATCH_BYTES = 12 << 20
 BLOCK_SIZE, HEAD_DIM, MAX_GROUP = 16, 128, 8
 
 _DTYPE_CODE = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16, torch.float32: PA_FP32}
@@ -49,6 +51,7 @@ def _load():
         "pa_decode_workspace_bytes": (sz, [vp, i32, i32, i32, i32]),
         "pa_decode_split": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
         "pa_append_decode": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
+        "pa_decode_split_static": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp]),
         "pa_copy_blocks": (i32, [vp, vp, vp, i32, vp]),
         "pa_check": (i32, [vp, vp, ctypes.POINTER(i64)]),
         "pa_profile_start": (i32, [i32]),
@@ -209,6 +212,15 @@ def pa_decode_split(pool, q, block_tables, seq_lens, scale, out, partition_block
                                float(scale), _ptr(out), _DTYPE_CODE[out.dtype], int(partition_blocks),
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream)), "pa_decode_split")
+
+
+def pa_decode_split_static(pool, q, block_tables, seq_lens, scale, out, partition_blocks=0, stream=None):
+    """pa_decode_split without a caller workspace: uses the library's static
+    device scratch (see include/pa.h); allocates nothing."""
+    B, Hq, W = _decode_args(pool, q, block_tables, seq_lens, out)
+    _check(lib.pa_decode_split_static(pool.handle, _ptr(q), _ptr(block_tables), W, _ptr(seq_lens), B, Hq,
+                                      float(scale), _ptr(out), _DTYPE_CODE[out.dtype], int(partition_blocks),
+                                      _stream(stream)), "pa_decode_split_static")
 
 
 def pa_append_decode(pool, q, k_new, v_new, block_tables, seq_lens, scale, out, partition_blocks=0,

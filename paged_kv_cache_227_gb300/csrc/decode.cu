@@ -1137,4 +1137,57 @@ int pa_append_decode(pa_pool_t p, const void* q, const void* k_new, const void* 
                        workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Split decode without allocation: the workspace is this file's static device
+// array.  For callers that cannot allocate device memory when they decode.
+// ---------------------------------------------------------------------------
 }  // extern "C"
+
+namespace pa {
+
+static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on `device` (the host-side symbol is
+// only a stand-in).  Looked up once per device with that device current.
+static int static_scratch_on(int device, void** out) {
+  static std::mutex mu;
+  static std::vector<void*> addr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0) return PA_ERR_INVALID;
+  if (static_cast<size_t>(device) >= addr.size()) addr.resize(device + 1, nullptr);
+  if (!addr[device]) {
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return PA_ERR_CUDA;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return PA_ERR_CUDA;
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess || !ptr) return PA_ERR_CUDA;
+    addr[device] = ptr;
+  }
+  *out = addr[device];
+  return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" int pa_decode_split_static(pa_pool_t p, const void* q, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                      int n_q_heads, float scale, void* out, int out_dtype,
+                                      int partition_blocks, void* stream) {
+  if (!p || partition_blocks < 0) return PA_ERR_INVALID;
+  WorkspaceLayout lay{};
+  if (!workspace_layout(p, num_seqs, n_q_heads, max_blocks_per_seq, partition_blocks, &lay))
+    return PA_ERR_INVALID;
+  if (lay.total > static_cast<size_t>(PA_STATIC_SCRATCH_BYTES)) return PA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  int st = static_scratch_on(p->device, &scratch);
+  if (st != PA_OK) return st;
+  // the per-pair counters must start at zero; the records need no clearing
+  if (cudaMemsetAsync(static_cast<char*>(scratch) + lay.counters_offset, 0,
+                      lay.total - lay.counters_offset, as_stream(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return pa_decode_split(p, q, block_tables, max_blocks_per_seq, seq_lens, num_seqs, n_q_heads,
+                         scale, out, out_dtype, partition_blocks, scratch,
+                         static_cast<size_t>(PA_STATIC_SCRATCH_BYTES), stream);
+}

@@ -192,6 +192,7 @@ const char* pa_strerror(int code) {
     case PA_ERR_CUDA: return "CUDA runtime or launch failure";
     case PA_ERR_DEVICE_CHECK: return "a kernel met an out-of-range block id or slot and skipped it";
     case PA_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+    case PA_ERR_SCRATCH_LIMIT: return "the call needs more workspace than the library's static scratch holds";
     default: return "unknown status";
   }
 }
