@@ -1,0 +1,69 @@
+"""Host logic of the multi-process benchmark, on CPU with the gloo backend
+(world size 2): the job's time is the slowest rank's, its bytes the sum of
+the ranks' (weak scaling, every rank decodes its own batch), and under the
+launcher only rank 0 prints."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        sys.path.insert(0, ROOT)
+        import bench
+        times, total = bench.reduce_over_ranks([10.0 + rank, 7.0 - 3 * rank], 1000 * (rank + 1), "cpu")
+        results[rank] = (times, total)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_over_two_gloo_ranks():
+    world = 2
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        mp.start_processes(_rank_main, args=(world, _free_port(), results), nprocs=world,
+                           join=True, start_method="spawn")
+        got = dict(results)
+    for r in range(world):
+        times, total = got[r]
+        assert times == [11.0, 7.0], "each timing is the max over ranks"
+        assert total == 3000.0, "bytes are summed over ranks"
+
+
+def test_reduce_without_process_group_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    times, total = bench.reduce_over_ranks([1.5, 2.5], 42, "cpu")
+    assert times == [1.5, 2.5] and total == 42.0
+
+
+def test_reference_arm_prints_once_under_the_launcher():
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--workload", "1"]
+    p = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["value"] > 0
