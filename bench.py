@@ -208,7 +208,7 @@ def run_ours(args, rank, world, local):
             ctypes.c_void_p(sl.data_ptr()), q.shape[0], q.shape[1], float(case.scale),
             ctypes.c_void_p(out.data_ptr()), pa._DTYPE_CODE[out.dtype], args.partition_blocks,
             ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
-    launches_per_step = 1  # one decode launch; split segments merge inside it
+    launches_per_step = 2  # the decode kernel and the merge of split segments
 
     def step():
         code = fn(*argv)

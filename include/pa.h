@@ -145,20 +145,18 @@ size_t pa_decode_workspace_bytes(pa_pool_t pool, int num_seqs, int n_q_heads,
  * cut into partitions of partition_blocks blocks, and each (sequence, kv head,
  * partition) is one work unit.  partition_blocks == 0: the tiles of all
  * (sequence, kv head) pairs, laid end to end, are cut into equal ranges, one
- * per CTA of a persistent grid sized to the GPU, so any length mix is spread
- * evenly; a pair cut by a range boundary becomes several units.  A unit that
- * does not cover its whole pair writes its running max m, sum l and
- * unnormalised output o in fp32 to the workspace and counts itself done on
- * the pair's counter; the CTA that finishes the pair's last unit merges the
- * partial results by log-sum-exp in the same launch:
+ * per warp of a persistent grid sized to the GPU, so any length mix is
+ * spread evenly; a pair cut by a range boundary becomes several units.  A unit
+ * that does not cover its whole pair writes its running max m, sum l and
+ * unnormalised output o in fp32 to the workspace; a second kernel, launched
+ * on the same stream as a programmatic dependent of the first, merges each
+ * cut pair's partial results by log-sum-exp in their fixed order:
  *   M = max_p m_p,  out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
- * The result equals pa_decode's up to rounding.  Pairs covered by a single
- * unit are written directly.  workspace: device, at least
- * pa_decode_workspace_bytes(...) bytes, 16-byte aligned, caller-owned.  It
- * must be zero-filled before its first use; every call that returns PA_OK and
- * completes on the GPU leaves its counters at zero again (after a device
- * error, zero it again).  Calls that share a workspace must not overlap on
- * the GPU. */
+ * The result equals pa_decode's up to rounding and does not depend on
+ * timing.  Pairs covered by a single unit are written directly.  workspace:
+ * device, at least pa_decode_workspace_bytes(...) bytes, 16-byte aligned,
+ * caller-owned; its contents on entry do not matter.  Calls that share a
+ * workspace must not overlap on the GPU. */
 int pa_decode_split(pa_pool_t pool, const void* q, const int32_t* block_tables,
                     int max_blocks_per_seq, const int32_t* seq_lens,
                     int num_seqs, int n_q_heads, float scale, void* out,
@@ -196,9 +194,8 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
  *    exits.  The first call on a device looks the array's device address up
  *    (cudaGetSymbolAddress, with that device current) and caches it, so make
  *    the first call on each device before any stream capture.
- *  - All calls share the array and it keeps the last call's contents; the
- *    call clears the part that must start at zero (the per-pair counters)
- *    with an asynchronous memset on `stream`.  Calls that overlap on the GPU
+ *  - All calls share the array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero.  Calls that overlap on the GPU
  *    (two streams, or two devices' calls racing on one device's array) race
  *    on the array: serialise them.
  *  - No cudaMalloc, cudaFree or other allocating routine is called. */

@@ -200,7 +200,7 @@ def workspace_for(pool, q, block_tables, partition_blocks=0):
     n = pa_decode_workspace_bytes(pool, q.shape[0], q.shape[1], block_tables.shape[1], partition_blocks)
     if n == 0:
         raise PagedAttentionError(PA_ERR_INVALID, "pa_decode_workspace_bytes")
-    return torch.zeros(n, dtype=torch.uint8, device=q.device)  # counters start at zero
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
 def pa_decode_split(pool, q, block_tables, seq_lens, scale, out, partition_blocks=0,

@@ -20,25 +20,28 @@
 //              by a range boundary leaves partial results;
 //   PARTITION  fixed partitions of `partition_blocks` tiles per segment.
 // A piece that does not cover its whole segment writes a partial record
-// (running max m, sum l, unnormalised o, fp32) and counts itself done on the
-// segment's counter with an acquire-release atomic; the warp that completes
-// the count merges the records by log-sum-exp, writes the output and resets
-// the counter to zero.
+// (running max m, sum l, unnormalised o, fp32); a second kernel, launched as a
+// programmatic dependent of this one, merges each cut segment's records by
+// log-sum-exp in their fixed order.  Partial records need no fence, atomic or
+// counter, so no warp ever stalls on another warp's progress.
 //
 // Per warp: a private ring of S shared-memory stages.  The warp streams its
 // tiles in with TMA tensor loads (one 8 KiB box per tile: the K and the V
 // tile, each as two 16-row x 128-byte swizzled halves; completion on an
-// mbarrier) and refills a stage the
-// moment it has finished with it, so S-1 tiles are always in flight and no
-// warp ever waits on another.  Per tile:
+// mbarrier) and refills a stage the moment it has finished with it.  Per
+// tile (software-pipelined: the score product of tile j+1 is issued before
+// the value product of tile j):
 //   scores  S^T[t][g] = K[t] . q_g with mma.sync m16n8k16 (M = 16 tokens,
 //           N = 8 query heads of the group, 8 k-steps of 16 dims, fp32
 //           accumulate, 4 independent accumulators); ldmatrix reads the
 //           swizzled K tile without bank conflicts;
 //   online softmax in fp32 in the log2 domain with a lazily moved running
 //           max (rescale only when a new max exceeds the old by 2^8);
-//   values  o[g][:] += p[t][g] V[t][:] in fp32 on the FMA pipes (packed
-//           two-wide FMAs), with p exact in fp32 (no rounding of weights).
+//   values  for G <= 4, O^T += V^T P with mma.sync (M = 128 dims in 8
+//           m-tiles read by ldmatrix.trans, N = 8 columns holding the high
+//           and the low 16-bit halves of each head's weights, so the weights
+//           keep ~17 bits; fp32 accumulate); for G > 4, o[g][:] +=
+//           p[t][g] V[t][:] in fp32 on the FMA pipes (packed two-wide FMAs).
 // Positions t >= L are masked by select in the scores and skipped in the
 // values, so padding or stale slots (even NaN) never reach the output.
 #include <cuda_bf16.h>
@@ -82,7 +85,6 @@ struct Params {
   const int32_t* seq_lens;  // [B]
   void* out;                // [B][Hq][128]
   float* ws;                // partial records
-  int* counters;            // [B][Hkv] pieces finished per segment (zero between calls)
   long long* err;
   long long num_blocks;
   int max_blocks;
@@ -152,6 +154,43 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// Transpose of an 8x8 16-bit matrix held one 32-bit pair per lane (lane t:
+// row t/4, columns 2(t%4), 2(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// Two fp32 values as a 16-bit pair (a in the low half), rounded to nearest;
+// pack_lo packs what rounding left over, so hi + lo carries a to ~2^-17.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack_hi(float a, float b) {
+  if (kBf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack_lo(float a, float b) {
+  if (kBf16) {
+    const float ra = a - __bfloat162float(__float2bfloat16_rn(a));
+    const float rb = b - __bfloat162float(__float2bfloat16_rn(b));
+    __nv_bfloat162 h = __floats2bfloat162_rn(ra, rb);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  const float ra = a - __half2float(__float2half_rn(a));
+  const float rb = b - __half2float(__float2half_rn(b));
+  __half2 h = __floats2half2_rn(ra, rb);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
 // D = A B + D for m16n8k16 (fp32 accumulate).
 template <bool kBf16>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -166,12 +205,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// Acquire-release add at GPU scope; returns the old value.
-__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
 }
 // Byte offset of 16-byte chunk c (0..15) of row r in a tile stored as two
 // 128-byte-swizzled boxes [16 rows][64 elements] (the TMA 128-byte swizzle
@@ -220,6 +253,22 @@ __device__ __forceinline__ void store_out(void* out, long long idx, float x, int
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(x);
   else
     static_cast<__half*>(out)[idx] = __float2half_rn(x);
+}
+
+// Four consecutive outputs starting at an index that is a multiple of 4.
+__device__ __forceinline__ void store_out4(void* out, long long idx, float a, float b, float c, float d,
+                                           int out_dtype) {
+  if (out_dtype == PA_FP32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = make_float4(a, b, c, d);
+  } else if (out_dtype == PA_BF16) {
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(a, b), h1 = __floats2bfloat162_rn(c, d);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
+  } else {
+    __half2 h0 = __floats2half2_rn(a, b), h1 = __floats2half2_rn(c, d);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
+  }
 }
 
 // Eight consecutive outputs starting at an index that is a multiple of 8.
@@ -272,15 +321,16 @@ struct Piece {
 
 struct PieceIter {
   const Params& P;
-  const int* pfx;  // shared: exclusive prefix over sequences (LEAN: tiles, PARTITION: partitions)
+  const int* pfx;   // shared: exclusive prefix over sequences (LEAN: tiles, PARTITION: partitions)
+  const int* lens;  // shared: clamped lengths (split schedules), or null (read from P.seq_lens)
   int unit, n_units;
   long long x, x_end;        // SEGMENT / PARTITION cursor
   long long cur, end;        // LEAN cursor
   int li, lh, lj;
   bool first;
 
-  __device__ PieceIter(const Params& p, const int* prefix, int u, int nu)
-      : P(p), pfx(prefix), unit(u), n_units(nu) {
+  __device__ PieceIter(const Params& p, const int* prefix, const int* lengths, int u, int nu)
+      : P(p), pfx(prefix), lens(lengths), unit(u), n_units(nu) {
     first = true;
     if (P.sched == SCHED_LEAN) {
       long long T = static_cast<long long>(P.Hkv) * pfx[P.B];
@@ -307,6 +357,8 @@ struct PieceIter {
     }
   }
 
+  __device__ int len(int i) const { return lens ? lens[i] : clamp_len(P, i); }
+
   __device__ bool next(Piece& pc) {
     if (P.sched == SCHED_LEAN) {
       if (cur >= end) return false;
@@ -318,7 +370,7 @@ struct PieceIter {
       pc.h = lh;
       pc.j0 = lj;
       pc.j1 = lj + static_cast<int>(pend - cur);
-      pc.L = clamp_len(P, li);
+      pc.L = len(li);
       pc.final_out = (lj == 0 && pend == seg_end);
       pc.rec = 2ll * unit + (first ? 0 : 1);
       first = false;
@@ -338,7 +390,7 @@ struct PieceIter {
     if (P.sched == SCHED_SEGMENT) {
       pc.i = static_cast<int>(x / P.Hkv);
       pc.h = static_cast<int>(x - static_cast<long long>(pc.i) * P.Hkv);
-      pc.L = clamp_len(P, pc.i);
+      pc.L = len(pc.i);
       pc.j0 = 0;
       pc.j1 = (pc.L + kBlock - 1) / kBlock;
       pc.final_out = true;
@@ -352,7 +404,7 @@ struct PieceIter {
         if (pfx[mid] <= u) lo = mid; else hi = mid - 1;
       }
       pc.i = lo;
-      pc.L = clamp_len(P, lo);
+      pc.L = len(lo);
       int nb = (pc.L + kBlock - 1) / kBlock;
       int p = static_cast<int>(u - pfx[lo]);
       pc.j0 = p * P.partition_blocks;
@@ -389,6 +441,44 @@ struct SegmentRecords {
   }
 };
 
+// Exclusive prefix over sequences of the per-sequence counts (tiles for
+// LEAN, partitions for PARTITION) into pfx[0..B], and, when lens is given, the
+// clamped lengths into lens[0..B).  All threads of the block load the
+// lengths; warp 0 scans.  Ends with a block barrier.
+__device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cap = P.max_blocks * kBlock;
+  for (int i = threadIdx.x; i < P.B; i += blockDim.x) {
+    int L = P.seq_lens[i];
+    if (L < 0 || L > cap) {
+      if (report) record_error(P.err, PA_ERR_DEVICE_CHECK, static_cast<long long>(L));
+      L = L < 0 ? 0 : cap;
+    }
+    if (lens) lens[i] = L;
+    const int nb = (L + kBlock - 1) / kBlock;
+    pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < P.B; base += 32) {
+      const int i = base + lane;
+      const int c = i < P.B ? pfx[i + 1] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      __syncwarp();
+      if (i < P.B) pfx[i + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pfx[0] = 0;
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Shared memory.  The rings come first at a 1024-byte aligned base (the
 // 128-byte swizzle of TMA boxes needs it); p buffers are 16-byte aligned.
@@ -402,7 +492,7 @@ struct __align__(1024) Smem {
   __align__(8) unsigned long long full[NW][SW];
   int stage_blk[NW][SW];
   int abort_flag;
-  int pfx[1];  // [B + 1], dynamic tail
+  int pfx[1];  // dynamic tail: prefix [B + 1], then clamped lengths [B]
 };
 
 template <int G>
@@ -419,7 +509,7 @@ static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() 
 // to align the base to 1024 bytes.
 template <int G>
 constexpr size_t smem_bytes(int B) {
-  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>(B + 1) + 1024;
+  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>(2 * B + 1) + 1024;
 }
 
 // ---------------------------------------------------------------------------
@@ -443,36 +533,10 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (P.sched != SCHED_SEGMENT) {
-    // exclusive prefix of per-sequence counts (tiles for LEAN, partitions for
-    // PARTITION): all threads fetch the counts, then warp 0 scans them
-    const int cap = P.max_blocks * kBlock;
-    for (int i = threadIdx.x; i < P.B; i += blockDim.x) {
-      int L = P.seq_lens[i];
-      L = L < 0 ? 0 : (L > cap ? cap : L);
-      int nb = (L + kBlock - 1) / kBlock;
-      S.pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int carry = 0;
-      for (int base = 0; base < P.B; base += 32) {
-        int i = base + lane;
-        int c = i < P.B ? S.pfx[i + 1] : 0;
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        __syncwarp();
-        if (i < P.B) S.pfx[i + 1] = carry + incl;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) S.pfx[0] = 0;
-    }
-  }
   __syncthreads();
+  if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0);
+  // the merge kernel that follows may start its own set-up now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // zero rows of empty sequences (split schedules; SEGMENT pieces write them)
   if (P.sched != SCHED_SEGMENT) {
@@ -484,6 +548,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   }
 
   volatile int* abort_flag = &S.abort_flag;
+  const int* S_lens = P.sched != SCHED_SEGMENT ? S.pfx + P.B + 1 : nullptr;
   const int unit = blockIdx.x * NW + warp;
   const int n_units = gridDim.x * NW;
   uint8_t* ring = S.stage[warp][0];
@@ -498,32 +563,70 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   // ldmatrix: lane group lm supplies matrix lm, row lr: [tok 0-7 | 8-15] x [chunk +0 | +1]
   const int lm = lane >> 3, lr = lane & 7;
   const int k_tok = lr + 8 * (lm & 1), k_cadd = lm >> 1;
+  // ldmatrix.trans of V^T: matrix lm covers tokens 8*(lm/2).. and dims 8*(lm%2).. of an m-tile
+  const int v_tok = lr + 8 * (lm >> 1), v_cadd = lm & 1;
+  // value product on the tensor cores when the high and low weight halves of
+  // all heads fit the 8 columns of one m16n8k16 product
+  constexpr bool kMmaPv = G <= 4;
   // value phase: lane owns 16-byte chunk c16 of the V rows of token parity r16
   const int c16 = lane & 15;
   const int r16 = lane >> 4;
 
-  // ---- issue side: walks the piece list up to SW tiles ahead ---------------
-  PieceIter iss(P, S.pfx, unit, n_units);
-  Piece ip;
+  // ---- issue side: walks the piece list SW tiles ahead of the consumer.
+  // Block ids come from 32-entry windows of a piece's table row held one per
+  // lane; the window after the current one (the rest of this piece, or the
+  // first of the next piece) is already being loaded, so an issue never waits
+  // on the table.  Entering a piece also prefetches the piece after it's q
+  // rows (and new K/V rows) into L2.
+  PieceIter iss(P, S.pfx, S_lens, unit, n_units);
+  Piece ip, inx;  // current and next piece of the issue side
   bool ihave = iss.next(ip);
+  bool inx_have = ihave && iss.next(inx);
   int ij = ihave ? ip.j0 : 0;
-  bool tb_ok = false;
-  int tb_base = 0, tb_val = 0;
+  int tb_base = ij, tb_val = 0, tb_nv = 0;
   int n_issued = 0;
+  auto window = [&](const Piece& pp, int base) -> int {
+    const int jj = base + lane;
+    return jj < pp.j1 ? P.tables[static_cast<long long>(pp.i) * P.max_blocks + jj] : 0;
+  };
+  auto prefetch_rows = [&](const Piece& pp) {
+    const long long qrow = (static_cast<long long>(pp.i) * P.Hq + pp.h * G) * kHeadDim;
+    if (lane < 2 * G) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + qrow + 64 * lane));
+    } else if (kFused && lane < 2 * G + 4) {
+      const int r = lane - 2 * G;
+      const long long nrow = (static_cast<long long>(pp.i) * P.Hkv + pp.h) * kHeadDim + 64 * (r & 1);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"((r < 2 ? P.k_new : P.v_new) + nrow));
+    }
+  };
+  auto load_following = [&]() {
+    if (tb_base + 32 < ip.j1) {
+      tb_nv = window(ip, tb_base + 32);
+    } else if (inx_have) {
+      tb_nv = window(inx, inx.j0);
+      prefetch_rows(inx);
+    }
+  };
+  if (ihave) {
+    tb_val = window(ip, ij);
+    load_following();
+  }
   auto issue = [&](int stage) {
-    while (ihave && ij >= ip.j1) {
-      ihave = iss.next(ip);
-      if (ihave) {
-        ij = ip.j0;
-        tb_ok = false;
-      }
+    while (ihave && ij >= ip.j1) {  // enter the next piece: its first window is tb_nv
+      ip = inx;
+      ihave = inx_have;
+      if (!ihave) return;
+      inx_have = iss.next(inx);
+      ij = ip.j0;
+      tb_base = ij;
+      tb_val = tb_nv;
+      load_following();
     }
     if (!ihave) return;
-    if (!tb_ok || ij - tb_base >= 32) {  // warp-uniform: refresh 32 table entries
-      tb_base = ij;
-      tb_ok = true;
-      const int jj = ij + lane;
-      tb_val = jj < ip.j1 ? P.tables[static_cast<long long>(ip.i) * P.max_blocks + jj] : 0;
+    if (ij - tb_base >= 32) {  // the next window of the same piece
+      tb_base += 32;
+      tb_val = tb_nv;
+      load_following();
     }
     const int blk = __shfl_sync(0xffffffffu, tb_val, ij - tb_base);
     if (lane == 0) {
@@ -543,7 +646,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     ++n_issued;
   };
   // ---- consume side -----------------------------------------------------------
-  PieceIter cit(P, S.pfx, unit, n_units);
+  PieceIter cit(P, S.pfx, S_lens, unit, n_units);
   Piece pc;
   bool have_pc = cit.next(pc);
   // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
@@ -562,7 +665,19 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
     }
   };
-  if (have_pc) load_q();  // in flight while the first loads are issued
+  // fused append: this lane's 16 bytes of the new K (lanes 0-15) or V row,
+  // fetched when the piece that holds the sequence's last tile starts
+  uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+  auto load_new = [&]() {
+    if (kFused && pc.L > 0 && pc.j1 == (pc.L + kBlock - 1) / kBlock) {
+      const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
+      newrow = *reinterpret_cast<const uint4*>((lane < 16 ? P.k_new : P.v_new) + src + 8 * c16);
+    }
+  };
+  if (have_pc) {  // in flight while the first loads are issued
+    load_q();
+    load_new();
+  }
 #pragma unroll 1
   for (int s = 0; s < SW; ++s) issue(s);
 
@@ -570,19 +685,27 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   bool ok = true;
   float (*pb)[PB] = S.pbuf[warp];
   while (ok && have_pc) {
-    float2 o[G][4];
+    // value accumulators.  Tensor-core path (G <= 4): oc[mt] is the m16n8
+    // fragment of O^T for dims 16mt..16mt+15: this lane holds dims 16mt+r4
+    // and 16mt+r4+8 of columns 2c4, 2c4+1, where columns 0-3 accumulate the
+    // high halves and columns 4-7 the low halves of the weights of heads 0-3.
+    // FMA path (G > 4): o[g][e] holds dims 8*c16+2e, +1 of head g over the
+    // tokens of parity r16.
+    float oc[kMmaPv ? 8 : 1][4];
+    float2 o[kMmaPv ? 1 : G][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int mt = 0; mt < (kMmaPv ? 8 : 1); ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+#pragma unroll
+    for (int g = 0; g < (kMmaPv ? 1 : G); ++g)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     const int nb_total = (pc.L + kBlock - 1) / kBlock;
 
-    // ---- tile loop, software-pipelined: the score product of tile j+1 is
-    // issued before the value product of tile j, so tensor-core latency hides
-    // behind the FMA work.
-    // prepare(): wait for the tile's stage, read its block id, and for the
-    // fused append put the new token into the tile and the pool.
+    // prepare(): wait for the tile's stage, read its block id, put the new
+    // token into the tile and the pool (fused append), and on the tensor-core
+    // path clear the V rows past the sequence's end (0 x NaN would poison
+    // the product; the weights there are exactly zero).
     auto prepare = [&](int jj, int nn, int& blk_out, bool& touched_out) -> bool {
       const int s = nn % SW;
       const uint32_t parity = static_cast<uint32_t>((nn / SW) & 1);
@@ -593,20 +716,25 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       if (!got) return false;
       const int blk = S.stage_blk[warp][s];
       blk_out = blk;
-      if (blk >= 0 && kFused && jj == nb_total - 1) {
-        // the new token: use the caller's k_new/v_new for position L-1 and
-        // write it to its slot in the pool
+      if (blk >= 0 && jj == nb_total - 1) {
         uint8_t* Ks = ring + s * kStageBytes;
-        const int tn = (pc.L - 1) & (kBlock - 1);
-        const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
-        const long long dst = ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
-        const uint16_t* from = (lane < 16 ? P.k_new : P.v_new) + src;
-        uint4 val = *reinterpret_cast<const uint4*>(from + 8 * c16);
-        *reinterpret_cast<uint4*>((lane < 16 ? Ks : Ks + kTileBytes) + swz(tn, c16)) = val;
-        uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
-        *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = val;
-        touched_out = true;
-        __syncwarp();
+        if (kFused) {
+          // the new token: the caller's k_new/v_new for position L-1, also
+          // written to its slot in the pool
+          const int tn = (pc.L - 1) & (kBlock - 1);
+          const long long dst = ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
+          *reinterpret_cast<uint4*>((lane < 16 ? Ks : Ks + kTileBytes) + swz(tn, c16)) = newrow;
+          uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
+          *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = newrow;
+          touched_out = true;
+        }
+        const int valid = pc.L - jj * kBlock;
+        if (kMmaPv && valid < kBlock) {
+          for (int x = valid * 16 + lane; x < kBlock * 16; x += 32)
+            *reinterpret_cast<uint4*>(Ks + kTileBytes + swz(x >> 4, x & 15)) = make_uint4(0u, 0u, 0u, 0u);
+          touched_out = true;
+        }
+        if (touched_out) __syncwarp();
       }
       return true;
     };
@@ -636,6 +764,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       const int s = n % SW;
       const uint8_t* Vs = ring + s * kStageBytes + kTileBytes;
       const int valid_tokens = pc.L - j * kBlock < kBlock ? pc.L - j * kBlock : kBlock;
+      float p[4];
       if (cur_blk >= 0) {
         float st[4];
 #pragma unroll
@@ -660,31 +789,46 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
             l_run[c] *= alpha[c];
             m_run[c] = mn;
           }
+          if constexpr (kMmaPv) {
+            // columns 4-7 (low halves) belong to the heads of lane c4 - 2
+            const float x0 = __shfl_xor_sync(0xffffffffu, alpha[0], 2);
+            const float x1 = __shfl_xor_sync(0xffffffffu, alpha[1], 2);
+            const float a0 = c4 < 2 ? alpha[0] : x0, a1 = c4 < 2 ? alpha[1] : x1;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float al = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
+            for (int mt = 0; mt < 8; ++mt) {
+              oc[mt][0] *= a0;
+              oc[mt][1] *= a1;
+              oc[mt][2] *= a0;
+              oc[mt][3] *= a1;
+            }
+          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              o[g][e].x *= al;
-              o[g][e].y *= al;
+            for (int g = 0; g < (kMmaPv ? 1 : G); ++g) {
+              const float al = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                o[g][e].x *= al;
+                o[g][e].y *= al;
+              }
             }
           }
         }
-        float p[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           p[k] = fast_exp2(st[k] - m_run[k & 1]);
           l_run[k & 1] += p[k];
         }
-        if (g0 < G) {
-          pb[r4][g0] = p[0];
-          pb[r4 + 8][g0] = p[2];
+        if constexpr (!kMmaPv) {
+          if (g0 < G) {
+            pb[r4][g0] = p[0];
+            pb[r4 + 8][g0] = p[2];
+          }
+          if (g0 + 1 < G) {
+            pb[r4][g0 + 1] = p[1];
+            pb[r4 + 8][g0 + 1] = p[3];
+          }
+          __syncwarp();
         }
-        if (g0 + 1 < G) {
-          pb[r4][g0 + 1] = p[1];
-          pb[r4 + 8][g0 + 1] = p[3];
-        }
-        __syncwarp();
       }
       // ---- next tile: wait for it and issue its score product now
       int nxt_blk = -1;
@@ -696,9 +840,27 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
         else if (nxt_blk >= 0)
           scores((n + 1) % SW, acc2);
       }
-      // ---- o += p V over this lane's tokens (parity r16) and dims (chunk c16)
       if (cur_blk >= 0) {
-        if (valid_tokens == kBlock) {  // full tile: no per-token branch, loads hoisted
+        if constexpr (kMmaPv) {
+          // ---- O^T += V^T P on the tensor cores.  B operand: the weights as
+          // a 16-token x 8-column matrix (columns 0-3: high 16-bit halves of
+          // heads 0-3, columns 4-7: the low halves, so hi + lo carries p to
+          // about 2^-17), transposed from the score fragment by movmatrix.
+          const float x0 = __shfl_xor_sync(0xffffffffu, p[0], 2);
+          const float x1 = __shfl_xor_sync(0xffffffffu, p[1], 2);
+          const float x2 = __shfl_xor_sync(0xffffffffu, p[2], 2);
+          const float x3 = __shfl_xor_sync(0xffffffffu, p[3], 2);
+          const uint32_t w01 = c4 < 2 ? pack_hi<kBf16>(p[0], p[1]) : pack_lo<kBf16>(x0, x1);
+          const uint32_t w23 = c4 < 2 ? pack_hi<kBf16>(p[2], p[3]) : pack_lo<kBf16>(x2, x3);
+          const uint32_t b0 = movmatrix_trans(w01), b1 = movmatrix_trans(w23);
+          const uint32_t vs_addr = smem_addr(Vs);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(vs_addr + swz(v_tok, 2 * mt + v_cadd), a0, a1, a2, a3);
+            mma16816<kBf16>(oc[mt], a0, a1, a2, a3, b0, b1);
+          }
+        } else if (valid_tokens == kBlock) {  // ---- o += p V on the FMA pipes, full tile
           uint4 raw[kBlock / 2];
           float pp[kBlock / 2][PB];
 #pragma unroll
@@ -716,7 +878,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
             float2 vf[4];
             unpack8<kBf16>(raw[k], vf);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < (kMmaPv ? 1 : G); ++g) {
               const float2 p2 = make_float2(pp[k][g], pp[k][g]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) o[g][e] = __ffma2_rn(p2, vf[e], o[g][e]);
@@ -737,7 +899,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
                 pp[g4] = q4.x; pp[g4 + 1] = q4.y; pp[g4 + 2] = q4.z; pp[g4 + 3] = q4.w;
               }
 #pragma unroll
-              for (int g = 0; g < G; ++g) {
+              for (int g = 0; g < (kMmaPv ? 1 : G); ++g) {
                 const float2 p2 = make_float2(pp[g], pp[g]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[g][e] = __ffma2_rn(p2, vf[e], o[g][e]);
@@ -759,14 +921,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     }
     if (!ok) break;
 
-    // ---- finish the piece: combine the token parities, then output or record
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, 16);
-        o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, 16);
-      }
+    // ---- finish the piece: per-head m and l, then the output row or a
+    // partial record
     float lsum[2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -781,30 +937,71 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       lg[g] = __shfl_sync(0xffffffffu, lsum[g & 1], g >> 1);
     }
     const long long row0 = (static_cast<long long>(pc.i) * P.Hq + pc.h * G) * kHeadDim;
-    if (pc.final_out) {
-      if (lane < 16) {
+    float* rec = P.ws + pc.rec * record_floats(G);
+    if constexpr (kMmaPv) {
+      // o = high + low columns; lanes c4 and c4^2 then hold the same sums:
+      // lane c4 < 2 writes dims 16mt+r4, lane c4 >= 2 dims 16mt+r4+8, of
+      // heads 2(c4&1) and 2(c4&1)+1
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float inv = lg[g] > 0.f ? 1.f / lg[g] : 0.f;
-          float v[8];
+      for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[2 * e] = o[g][e].x * inv;
-            v[2 * e + 1] = o[g][e].y * inv;
+        for (int e = 0; e < 4; ++e) oc[mt][e] += __shfl_xor_sync(0xffffffffu, oc[mt][e], 2);
+      const int hsel = (c4 & 1) * 2;
+      const int dadd = c4 < 2 ? 0 : 8;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int g = hsel + e;
+        if (g < G) {
+          float lgg = lg[0], mgg = mg[0];
+#pragma unroll
+          for (int gg = 1; gg < G; ++gg)
+            if (g == gg) {
+              lgg = lg[gg];
+              mgg = mg[gg];
+            }
+          (void)mgg;
+          const float inv = lgg > 0.f ? 1.f / lgg : 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const float v = c4 < 2 ? oc[mt][e] : oc[mt][2 + e];
+            const int d = 16 * mt + r4 + dadd;
+            if (pc.final_out)
+              store_out(P.out, row0 + g * kHeadDim + d, v * inv, P.out_dtype);
+            else
+              rec[g * kHeadDim + d] = v;
           }
-          store_out8(P.out, row0 + g * kHeadDim + 8 * c16, v, P.out_dtype);
         }
       }
     } else {
-      float* rec = P.ws + pc.rec * record_floats(G);
+      // combine the token parities
+#pragma unroll
+      for (int g = 0; g < (kMmaPv ? 1 : G); ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, 16);
+          o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, 16);
+        }
       if (lane < 16) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float4* dst = reinterpret_cast<float4*>(rec + g * kHeadDim + 8 * c16);
-          dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
-          dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
+        for (int g = 0; g < (kMmaPv ? 1 : G); ++g) {
+          if (pc.final_out) {
+            const float inv = lg[g] > 0.f ? 1.f / lg[g] : 0.f;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[2 * e] = o[g][e].x * inv;
+              v[2 * e + 1] = o[g][e].y * inv;
+            }
+            store_out8(P.out, row0 + g * kHeadDim + 8 * c16, v, P.out_dtype);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(rec + g * kHeadDim + 8 * c16);
+            dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
+            dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
+          }
         }
       }
+    }
+    if (!pc.final_out) {
       if (lane == 0) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -812,83 +1009,12 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
           rec[G * kHeadDim + 64 + g] = lg[g];
         }
       }
-      // ---- log-sum-exp merge by the warp that completes the segment:
-      //   M = max_p m_p;  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p
-      __syncwarp();
-      const SegmentRecords recs(P, S.pfx, pc.i, pc.h);
-      int* counter = P.counters + static_cast<long long>(pc.i) * P.Hkv + pc.h;
-      int last = 0;
-      if (lane == 0) last = atom_add_acq_rel(counter, 1) == recs.count - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        // merge: lane k fetches record k's m and l (one round trip for up to
-        // 32 records at a time); the warp forms M = max m and the weights
-        // 2^(m_k - M); then every lane accumulates its 4 dims of every head
-        // over the records, whose 16-byte loads are independent and unrolled
-        __syncwarp();
-        float M[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) M[g] = -INFINITY;
-        for (int base = 0; base < recs.count; base += 32) {
-          const int k = base + lane;
-          const float* r = P.ws + (k < recs.count ? recs.at(P, k) : 0) * record_floats(G);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float mk = k < recs.count ? __ldcg(r + G * kHeadDim + g) : -INFINITY;
-#pragma unroll
-            for (int msk = 1; msk < 32; msk <<= 1) mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, msk));
-            M[g] = fmaxf(M[g], mk);
-          }
-        }
-        float Ls[G];
-        float4 Os[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          Ls[g] = 0.f;
-          Os[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int base = 0; base < recs.count; base += 32) {
-          const int k = base + lane;
-          const bool have = k < recs.count;
-          const float* r = P.ws + (have ? recs.at(P, k) : 0) * record_floats(G);
-          float w[G];
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            w[g] = have ? fast_exp2(__ldcg(r + G * kHeadDim + g) - M[g]) : 0.f;
-            float lw = have ? __ldcg(r + G * kHeadDim + 64 + g) * w[g] : 0.f;
-#pragma unroll
-            for (int msk = 1; msk < 32; msk <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, msk);
-            Ls[g] += lw;
-          }
-          const int cnt = recs.count - base < 32 ? recs.count - base : 32;
-#pragma unroll 8
-          for (int kk = 0; kk < cnt; ++kk) {
-            const float* rk = P.ws + recs.at(P, base + kk) * record_floats(G);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float wk = __shfl_sync(0xffffffffu, w[g], kk);
-              const float4 ok = __ldcg(reinterpret_cast<const float4*>(rk + g * kHeadDim) + lane);
-              Os[g].x = fmaf(ok.x, wk, Os[g].x);
-              Os[g].y = fmaf(ok.y, wk, Os[g].y);
-              Os[g].z = fmaf(ok.z, wk, Os[g].z);
-              Os[g].w = fmaf(ok.w, wk, Os[g].w);
-            }
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float inv = Ls[g] > 0.f ? 1.f / Ls[g] : 0.f;
-          const long long idx = row0 + g * kHeadDim + 4 * lane;
-          store_out(P.out, idx, Os[g].x * inv, P.out_dtype);
-          store_out(P.out, idx + 1, Os[g].y * inv, P.out_dtype);
-          store_out(P.out, idx + 2, Os[g].z * inv, P.out_dtype);
-          store_out(P.out, idx + 3, Os[g].w * inv, P.out_dtype);
-        }
-        if (lane == 0) *counter = 0;
-      }
     }
     have_pc = cit.next(pc);
-    if (have_pc) load_q();
+    if (have_pc) {
+      load_q();
+      load_new();
+    }
   }
 
   // --- drain: never leave a bulk copy in flight into this warp's ring -------
@@ -902,6 +1028,88 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     }
   }
   __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// The merge kernel: the log-sum-exp combination of the partial records of
+// every segment that the decode kernel split (one warp per query head of a
+// segment, records in their fixed order, so the result does not depend on
+// timing):  M = max_p m_p;  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
+// It is launched as a programmatic dependent of the decode kernel: its
+// set-up (the prefix over the lengths, which are inputs) overlaps the decode
+// kernel's tail, and griddepcontrol.wait holds it until the decode kernel has
+// completed and its records are visible.
+// ---------------------------------------------------------------------------
+constexpr int kMergeThreads = 128;
+template <int G>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Params P) {
+  extern __shared__ int mpfx[];  // [B + 1]
+  block_prefix(P, mpfx, nullptr, false);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long long wpb = kMergeThreads / 32;
+  const long long n_items = static_cast<long long>(P.B) * P.Hkv * G;
+  constexpr int RB = 16;  // records whose o loads are in flight together
+  for (long long it = blockIdx.x * wpb + (threadIdx.x >> 5); it < n_items; it += gridDim.x * wpb) {
+    const int g = static_cast<int>(it % G);
+    const long long sh = it / G;
+    const int h = static_cast<int>(sh % P.Hkv);
+    const int i = static_cast<int>(sh / P.Hkv);
+    if (mpfx[i + 1] == mpfx[i]) continue;  // empty sequence: written by the decode kernel
+    const SegmentRecords recs(P, mpfx, i, h);
+    if (recs.count <= 1) continue;  // whole segment: written by the decode kernel
+    float M = -INFINITY, Ls = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < recs.count; c0 += 32) {
+      const int cnt = recs.count - c0 < 32 ? recs.count - c0 : 32;
+      const bool have = lane < cnt;
+      const float* rl = P.ws + recs.at(P, c0 + (have ? lane : 0)) * record_floats(G);
+      const float mv = __ldcg(rl + G * kHeadDim + g);
+      const float lv = __ldcg(rl + G * kHeadDim + 64 + g);
+      const float mk = have ? mv : -INFINITY;
+      const float lk = have ? lv : 0.f;
+      float wk = 0.f;
+      for (int b0 = 0; b0 < cnt; b0 += RB) {
+        float4 ob[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const int k = b0 + r < cnt ? b0 + r : 0;
+          ob[r] = __ldcg(reinterpret_cast<const float4*>(P.ws + recs.at(P, c0 + k) * record_floats(G) +
+                                                         g * kHeadDim) + lane);
+        }
+        if (b0 == 0) {  // this chunk's weights; rescale what came before
+          float mx = mk;
+#pragma unroll
+          for (int msk = 1; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+          const float mn = fmaxf(M, mx);
+          const float a = fast_exp2(M - mn);
+          wk = fast_exp2(mk - mn);
+          float lw = wk * lk;
+#pragma unroll
+          for (int msk = 1; msk < 32; msk <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, msk);
+          Ls = Ls * a + lw;
+          O.x *= a;
+          O.y *= a;
+          O.z *= a;
+          O.w *= a;
+          M = mn;
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const float w = __shfl_sync(0xffffffffu, wk, (b0 + r) & 31);
+          if (b0 + r < cnt) {
+            O.x = fmaf(w, ob[r].x, O.x);
+            O.y = fmaf(w, ob[r].y, O.y);
+            O.z = fmaf(w, ob[r].z, O.z);
+            O.w = fmaf(w, ob[r].w, O.w);
+          }
+        }
+      }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    const long long idx = (static_cast<long long>(i) * P.Hq + h * G + g) * kHeadDim + 4 * lane;
+    store_out4(P.out, idx, O.x * inv, O.y * inv, O.z * inv, O.w * inv, P.out_dtype);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -969,6 +1177,26 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
   if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
   decode_kernel<G, kBf16, kFused><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (P.sched != SCHED_SEGMENT) {
+    // the merge of split segments, as a programmatic dependent launch
+    constexpr long long kWarpsPerCta = kMergeThreads / 32;
+    long long items = static_cast<long long>(P.B) * P.Hkv * G;
+    long long mgrid = (items + kWarpsPerCta - 1) / kWarpsPerCta;
+    const long long mcap = static_cast<long long>(sm_count(device)) * 8;
+    if (mgrid > mcap) mgrid = mcap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(mgrid));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = sizeof(int) * static_cast<size_t>(P.B + 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, merge_kernel<G>, P) != cudaSuccess) return PA_ERR_CUDA;
+  }
   if (timed) {
     if (cudaEventRecord(g_prof_events[2 * g_prof_next + 1], stream) != cudaSuccess) return PA_ERR_CUDA;
     ++g_prof_next;
@@ -991,10 +1219,9 @@ static int launch_g(int G, Params& P, int device, cudaStream_t stream) {
   }
 }
 
-// Workspace layout: partial records, then the per-segment counters at a
-// 256-byte aligned offset.
+// Workspace layout: the partial records.
 struct WorkspaceLayout {
-  size_t records_bytes, counters_offset, total;
+  size_t records_bytes, total;
 };
 
 static bool workspace_layout(const pa_pool* p, int B, int Hq, int max_blocks, int partition_blocks,
@@ -1011,8 +1238,7 @@ static bool workspace_layout(const pa_pool* p, int B, int Hq, int max_blocks, in
     n_rec = static_cast<size_t>(B) * p->n_kv_heads *
             ((max_blocks + partition_blocks - 1) / partition_blocks);
   out->records_bytes = rec * n_rec;
-  out->counters_offset = (out->records_bytes + 255) / 256 * 256;
-  out->total = out->counters_offset + sizeof(int) * static_cast<size_t>(B) * p->n_kv_heads;
+  out->total = out->records_bytes;
   return true;
 }
 
@@ -1047,7 +1273,6 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.seq_lens = seq_lens;
   P.out = out;
   P.ws = static_cast<float*>(ws);
-  P.counters = ws ? reinterpret_cast<int*>(static_cast<char*>(ws) + lay.counters_offset) : nullptr;
   P.err = p->err;
   P.num_blocks = p->num_blocks;
   P.max_blocks = max_blocks;
@@ -1183,10 +1408,7 @@ extern "C" int pa_decode_split_static(pa_pool_t p, const void* q, const int32_t*
   void* scratch = nullptr;
   int st = static_scratch_on(p->device, &scratch);
   if (st != PA_OK) return st;
-  // the per-pair counters must start at zero; the records need no clearing
-  if (cudaMemsetAsync(static_cast<char*>(scratch) + lay.counters_offset, 0,
-                      lay.total - lay.counters_offset, as_stream(stream)) != cudaSuccess)
-    return PA_ERR_CUDA;
+  // nothing in the array needs clearing: every record is written before it is read
   return pa_decode_split(p, q, block_tables, max_blocks_per_seq, seq_lens, num_seqs, n_q_heads,
                          scale, out, out_dtype, partition_blocks, scratch,
                          static_cast<size_t>(PA_STATIC_SCRATCH_BYTES), stream);
