@@ -383,7 +383,7 @@ def main():
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_kernel (fused append + split decode)",
+            "kernel": "decode_kernel (fused append + split decode) + merge_kernel, one step",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
