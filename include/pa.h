@@ -285,6 +285,45 @@ int pa_alloc_refcount(pa_alloc_t a, int block);
 /* Number of blocks on the free list. */
 int pa_alloc_num_free(pa_alloc_t a);
 
+/* ---------------------------------------------------------------------------
+ * Prefix caching by block hashes ("Paged Attention" teaser on the
+ * inference-serving tag page: prefix caching by block hashes; the posts on
+ * the pagedattention tag: blocks chained by hashes, so one changed character
+ * early in a prompt voids every cached block after it).  Host only.
+ *
+ *  - A full block of a sequence whose tokens were all appended with their
+ *    ids is hashed when its last token arrives:
+ *      h_k = FNV-1a-64(h_{k-1} as 8 little-endian bytes ||
+ *                      its 16 token ids as 4-byte little-endian integers),
+ *    h_{-1} = 0 (FNV-1a: start 14695981039346656037; per byte: xor, then
+ *    multiply by 1099511628211 mod 2^64).  A hash already indexed keeps its
+ *    older block.  pa_alloc_append_slot (no id) stops hashing for that
+ *    sequence.
+ *  - The index keeps, per hash, the block, the parent hash and the 16 ids; a
+ *    lookup accepts an entry only if all three match (a collision misses).
+ *  - A block whose count drops to 0 joins the back of the free list and stays
+ *    indexed; a lookup that hits it takes it back off the free list; taking a
+ *    block from the front for a new allocation drops its index entry.
+ * ------------------------------------------------------------------------- */
+/* New sequence seq_id for a prompt of n_tokens ids (host array): shares the
+ * longest chain of cached full blocks from the prompt's start (counts +1) and
+ * stops at the first miss.  *n_cached (may be NULL) receives 16 x hits, the
+ * tokens the sequence now holds; append the rest with pa_alloc_append_token.
+ * INVALID if seq_id < 0 or exists, or tokens is NULL with n_tokens > 0. */
+int pa_alloc_seq_add_cached(pa_alloc_t a, int seq_id, const int32_t* tokens,
+                            int n_tokens, int* n_cached);
+/* pa_alloc_append_slot that also records the token's id; completing a block
+ * indexes it (see above). */
+int pa_alloc_append_token(pa_alloc_t a, int seq, int32_t token, int64_t* slot,
+                          int32_t* cow_src, int32_t* cow_dst);
+/* 1 and *hash = the block's hash if the block is indexed, 0 if not, or a
+ * negative status. */
+int pa_alloc_block_hash(pa_alloc_t a, int block, uint64_t* hash);
+/* Blocks looked up and hit by pa_alloc_seq_add_cached so far, and blocks now
+ * indexed (each pointer may be NULL). */
+int pa_alloc_prefix_stats(pa_alloc_t a, int64_t* queries, int64_t* hits,
+                          int64_t* cached_blocks);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,11 @@ def _load():
         "pa_alloc_seq_len": (i32, [vp, i32]),
         "pa_alloc_refcount": (i32, [vp, i32]),
         "pa_alloc_num_free": (i32, [vp]),
+        "pa_alloc_seq_add_cached": (i32, [vp, i32, vp, i32, ctypes.POINTER(i32)]),
+        "pa_alloc_append_token": (i32, [vp, i32, ctypes.c_int32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32),
+                                        ctypes.POINTER(ctypes.c_int32)]),
+        "pa_alloc_block_hash": (i32, [vp, i32, ctypes.POINTER(ctypes.c_uint64)]),
+        "pa_alloc_prefix_stats": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -313,6 +318,38 @@ class BlockAllocator:
             raise MemoryError(f"no free block after {done.value} tokens")
         _check(code, "pa_alloc_extend")
         return slots[:n], (cs.value, cd.value)
+
+    def seq_add_cached(self, seq, tokens):
+        """New sequence sharing the cached full blocks of `tokens` (a prompt of
+        token ids); returns the number of tokens it now holds."""
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        n = ctypes.c_int()
+        _check(lib.pa_alloc_seq_add_cached(self._h, seq, arr.ctypes.data_as(ctypes.c_void_p) if arr.size else None,
+                                           int(arr.size), ctypes.byref(n)), "pa_alloc_seq_add_cached")
+        return n.value
+
+    def append_token(self, seq, token):
+        slot, cs, cd = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        code = lib.pa_alloc_append_token(self._h, seq, int(token), ctypes.byref(slot), ctypes.byref(cs),
+                                         ctypes.byref(cd))
+        if code == PA_ERR_OOM:
+            raise MemoryError("no free block")
+        _check(code, "pa_alloc_append_token")
+        return slot.value, cs.value, cd.value
+
+    def block_hash(self, block):
+        h = ctypes.c_uint64()
+        r = lib.pa_alloc_block_hash(self._h, block, ctypes.byref(h))
+        if r < 0:
+            _check(r, "pa_alloc_block_hash")
+        return h.value if r == 1 else None
+
+    def prefix_stats(self):
+        q, h, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.pa_alloc_prefix_stats(self._h, ctypes.byref(q), ctypes.byref(h), ctypes.byref(c)),
+               "pa_alloc_prefix_stats")
+        return q.value, h.value, c.value
 
     def seq_free(self, seq):
         _check(lib.pa_alloc_seq_free(self._h, seq), "pa_alloc_seq_free")

@@ -4,29 +4,104 @@
 // from positions to blocks, and sequences that share a prefix share its
 // blocks ("Serving", section 23.4 Paged Attention); a write into a shared
 // block copies it first ("Paged Attention: Managing the KV Cache Like Virtual
-// Memory", inference-serving tag page).  The policy is spelled out in pa.h.
-#include <deque>
+// Memory", inference-serving tag page).  Full blocks can also be found again
+// by the chained hash of their tokens (prefix caching by block hashes, same
+// page; hash chains, posts on the pagedattention tag).  The policy is spelled
+// out in pa.h.
+#include <array>
+#include <cstring>
+#include <list>
 #include <unordered_map>
 #include <vector>
 
 #include "pa.h"
 
+namespace {
+
+// FNV-1a, 64-bit: offset basis 14695981039346656037, prime 1099511628211.
+uint64_t fnv1a64(const unsigned char* p, size_t n) {
+  uint64_t h = 14695981039346656037ull;
+  for (size_t k = 0; k < n; ++k) {
+    h ^= p[k];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+// Chained hash of a full block: the parent's hash as 8 little-endian bytes,
+// then the token ids as 4-byte little-endian integers.
+uint64_t block_hash(uint64_t parent, const int32_t* tok, int n) {
+  std::vector<unsigned char> buf(8 + 4 * static_cast<size_t>(n));
+  for (int k = 0; k < 8; ++k) buf[k] = static_cast<unsigned char>(parent >> (8 * k));
+  for (int t = 0; t < n; ++t) {
+    const uint32_t v = static_cast<uint32_t>(tok[t]);
+    for (int k = 0; k < 4; ++k) buf[8 + 4 * t + k] = static_cast<unsigned char>(v >> (8 * k));
+  }
+  return fnv1a64(buf.data(), buf.size());
+}
+
+}  // namespace
+
 struct pa_alloc {
   struct Seq {
     std::vector<int32_t> table;
     long long len = 0;
+    bool tracked = true;            // every token so far appended with its id
+    std::vector<int32_t> tokens;    // the ids (while tracked)
+    std::vector<uint64_t> chain;    // hashes of its full blocks (while tracked)
+  };
+  struct Entry {
+    int32_t block;
+    uint64_t parent;
+    std::vector<int32_t> tokens;
   };
   int num_blocks = 0;
   int block_size = 0;
-  std::deque<int32_t> free_list;
+  std::list<int32_t> free_list;  // FIFO; cached blocks can leave from the middle
+  std::vector<std::list<int32_t>::iterator> free_pos;
+  std::vector<char> on_free;
   std::vector<int32_t> refcount;
   std::unordered_map<int, Seq> seqs;
+  std::unordered_map<uint64_t, Entry> index;  // hash -> cached full block
+  std::vector<uint64_t> key_of;               // block -> its hash while indexed
+  std::vector<char> indexed;
+  long long queries = 0, hits = 0;
 
+  void push_free(int32_t b) {
+    free_list.push_back(b);
+    free_pos[b] = std::prev(free_list.end());
+    on_free[b] = 1;
+  }
   int take() {  // caller checked free_list is non-empty
     int32_t b = free_list.front();
     free_list.pop_front();
+    on_free[b] = 0;
+    if (indexed[b]) {  // the block is reused: its cached contents go away
+      index.erase(key_of[b]);
+      indexed[b] = 0;
+    }
     refcount[b] = 1;
     return b;
+  }
+  void share(int32_t b) {
+    if (refcount[b] == 0 && on_free[b]) {
+      free_list.erase(free_pos[b]);
+      on_free[b] = 0;
+    }
+    refcount[b] += 1;
+  }
+  // the block that just became full (block k of s) joins the index
+  void register_full(Seq& s, int k) {
+    const uint64_t parent = k > 0 ? s.chain[k - 1] : 0;
+    const int32_t* tok = s.tokens.data() + static_cast<size_t>(k) * block_size;
+    const uint64_t h = block_hash(parent, tok, block_size);
+    s.chain.push_back(h);
+    const int32_t b = s.table[k];
+    if (!index.count(h) && !indexed[b]) {
+      index.emplace(h, Entry{b, parent, std::vector<int32_t>(tok, tok + block_size)});
+      key_of[b] = h;
+      indexed[b] = 1;
+    }
   }
 
   int append(int seq, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
@@ -55,6 +130,17 @@ struct pa_alloc {
     if (cow_dst) *cow_dst = cd;
     return PA_OK;
   }
+
+  int append_token(int seq, int32_t token, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+    int st = append(seq, slot, cow_src, cow_dst);
+    if (st != PA_OK) return st;
+    Seq& s = seqs.find(seq)->second;
+    if (s.tracked) {
+      s.tokens.push_back(token);
+      if (s.tokens.size() % block_size == 0) register_full(s, static_cast<int>(s.tokens.size() / block_size) - 1);
+    }
+    return PA_OK;
+  }
 };
 
 extern "C" {
@@ -66,6 +152,10 @@ int pa_alloc_create(int num_blocks, int block_size, const int32_t* free_order, p
   a->num_blocks = num_blocks;
   a->block_size = block_size;
   a->refcount.assign(num_blocks, 0);
+  a->free_pos.resize(num_blocks);
+  a->on_free.assign(num_blocks, 0);
+  a->key_of.assign(num_blocks, 0);
+  a->indexed.assign(num_blocks, 0);
   if (free_order) {
     std::vector<char> seen(num_blocks, 0);
     for (int k = 0; k < num_blocks; ++k) {
@@ -75,10 +165,10 @@ int pa_alloc_create(int num_blocks, int block_size, const int32_t* free_order, p
         return PA_ERR_INVALID;  // not a permutation
       }
       seen[b] = 1;
-      a->free_list.push_back(b);
+      a->push_free(b);
     }
   } else {
-    for (int b = 0; b < num_blocks; ++b) a->free_list.push_back(b);
+    for (int b = 0; b < num_blocks; ++b) a->push_free(b);
   }
   *out = a;
   return PA_OK;
@@ -107,7 +197,62 @@ int pa_alloc_fork(pa_alloc_t a, int parent, int child) {
 
 int pa_alloc_append_slot(pa_alloc_t a, int seq, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
   if (!a) return PA_ERR_INVALID;
-  return a->append(seq, slot, cow_src, cow_dst);
+  int st = a->append(seq, slot, cow_src, cow_dst);
+  if (st == PA_OK) {
+    auto& s = a->seqs.find(seq)->second;
+    s.tracked = false;  // its token ids are unknown from here on
+    s.tokens.clear();
+    s.chain.clear();
+  }
+  return st;
+}
+
+int pa_alloc_append_token(pa_alloc_t a, int seq, int32_t token, int64_t* slot, int32_t* cow_src,
+                          int32_t* cow_dst) {
+  if (!a) return PA_ERR_INVALID;
+  return a->append_token(seq, token, slot, cow_src, cow_dst);
+}
+
+int pa_alloc_seq_add_cached(pa_alloc_t a, int seq_id, const int32_t* tokens, int n_tokens, int* n_cached) {
+  if (!a || seq_id < 0 || n_tokens < 0 || (n_tokens > 0 && !tokens) || a->seqs.count(seq_id))
+    return PA_ERR_INVALID;
+  pa_alloc::Seq s;
+  uint64_t parent = 0;
+  const int bs = a->block_size;
+  for (int k = 0; k + 1 <= n_tokens / bs; ++k) {
+    const int32_t* tok = tokens + static_cast<size_t>(k) * bs;
+    const uint64_t h = block_hash(parent, tok, bs);
+    a->queries += 1;
+    auto it = a->index.find(h);
+    if (it == a->index.end() || it->second.parent != parent ||
+        std::memcmp(it->second.tokens.data(), tok, sizeof(int32_t) * bs) != 0)
+      break;
+    a->hits += 1;
+    a->share(it->second.block);
+    s.table.push_back(it->second.block);
+    s.tokens.insert(s.tokens.end(), tok, tok + bs);
+    s.chain.push_back(h);
+    s.len += bs;
+    parent = h;
+  }
+  if (n_cached) *n_cached = static_cast<int>(s.len);
+  a->seqs.emplace(seq_id, std::move(s));
+  return PA_OK;
+}
+
+int pa_alloc_block_hash(pa_alloc_t a, int block, uint64_t* hash) {
+  if (!a || block < 0 || block >= a->num_blocks) return PA_ERR_INVALID;
+  if (!a->indexed[block]) return 0;
+  if (hash) *hash = a->key_of[block];
+  return 1;
+}
+
+int pa_alloc_prefix_stats(pa_alloc_t a, int64_t* queries, int64_t* hits, int64_t* cached_blocks) {
+  if (!a) return PA_ERR_INVALID;
+  if (queries) *queries = a->queries;
+  if (hits) *hits = a->hits;
+  if (cached_blocks) *cached_blocks = static_cast<int64_t>(a->index.size());
+  return PA_OK;
 }
 
 int pa_alloc_extend(pa_alloc_t a, int seq, int n, int64_t* slots, int32_t* cow_src,
@@ -135,7 +280,7 @@ int pa_alloc_seq_free(pa_alloc_t a, int seq) {
   auto it = a->seqs.find(seq);
   if (it == a->seqs.end()) return PA_ERR_INVALID;
   for (int32_t b : it->second.table) {
-    if (--a->refcount[b] == 0) a->free_list.push_back(b);
+    if (--a->refcount[b] == 0) a->push_free(b);
   }
   a->seqs.erase(it);
   return PA_OK;
