@@ -102,13 +102,18 @@ def assert_close(out, ref, what=""):
     return err
 
 
-FP32_FLOOR = 2e-6  # absolute error floor of the kernel's fp32 arithmetic
+# Absolute error floor of the native 16-bit check: the fp32 arithmetic
+# (2e-6), plus the value product's weights, which the tensor-core path (G <= 4)
+# carries as a high and a low 16-bit half, i.e. to 2^-18 relative; summed over
+# values |v| <= 6 (N(0,1) samples) that is at most 2^-18 * 6 per output.
+FP32_FLOOR = 2e-6 + 2.0 ** -18 * 6.0
 
 
 def assert_within_one_ulp16(out16, ref, dtype, what=""):
-    """Native 16-bit output: |out - RN16(ref)| <= 1 ulp of RN16(ref) + 2e-6.
+    """Native 16-bit output: |out - RN16(ref)| <= 1 ulp of RN16(ref) + FP32_FLOOR.
     The absolute term covers outputs so small that one 16-bit ulp (down to
-    2^-24 for fp16) is below the fp32 accumulation error."""
+    2^-24 for fp16) is below the kernel's own error (fp32 accumulation and
+    17-bit weights on the tensor-core value path)."""
     r16 = torch.from_numpy(ref).to(torch.float32).to(dtype).to(torch.float64).numpy()
     got = out16.detach().cpu().to(torch.float64).numpy().reshape(ref.shape)
     mant = 7 if dtype == torch.bfloat16 else 10
