@@ -177,6 +177,31 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
                      int out_dtype, int partition_blocks, void* workspace,
                      size_t workspace_bytes, void* stream);
 
+/* Attention for several new query tokens per sequence: a chunk of a prompt
+ * written onto the sequence's blocks, or drafted tokens checked in one pass
+ * ("Serving", sections 23.2 Prefill and Decode and 23.5 Speculative
+ * Decoding, over the blocks and tables of 23.4).  The new tokens' K/V must
+ * already be in the pool (pa_cache_append); seq_lens[i] counts them.
+ * q: device [n_q][n_q_heads][128]; sequence i's query rows are
+ * q_start[i] .. q_start[i+1]-1 (device int32 [num_seqs+1], non-decreasing,
+ * q_start[0] = 0, q_start[num_seqs] = n_q), its last T_i positions in order.
+ * Row r = q_start[i] + t sits at position L_i - T_i + t and attends over
+ * positions 0 .. L_i - T_i + t (causal within the new tokens):
+ *   out[r][h] = softmax(scale * K[0..p] q[r][h]) V[0..p],  p = L_i - T_i + t.
+ * out: device [n_q][n_q_heads][128] in out_dtype.  Each row is one unit of
+ * the balanced split (so the rows of a sequence read their common prefix
+ * close together in time; repeated reads are served from L2).  workspace:
+ * device, >= pa_decode_multi_workspace_bytes(...) bytes, 256-byte aligned.
+ * n_q <= 4096 (else PA_ERR_UNSUPPORTED).  A row with T_i > L_i, or a length
+ * out of range, records PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros. */
+size_t pa_decode_multi_workspace_bytes(pa_pool_t pool, int n_q, int n_q_heads,
+                                       int max_blocks_per_seq);
+int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n_q,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* seq_lens, int num_seqs, int n_q_heads,
+                    float scale, void* out, int out_dtype, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
 /* Split-KV decode that allocates nothing (the pages have no counterpart; this
  * is a deployment convenience).  Some callers cannot call cudaMalloc at the
  * time they decode: a serving loop whose device memory budget is fixed up

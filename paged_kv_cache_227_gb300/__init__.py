@@ -51,6 +51,8 @@ def _load():
         "pa_decode_workspace_bytes": (sz, [vp, i32, i32, i32, i32]),
         "pa_decode_split": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
         "pa_append_decode": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
+        "pa_decode_multi_workspace_bytes": (ctypes.c_size_t, [vp, i32, i32, i32]),
+        "pa_decode_multi": (i32, [vp, vp, vp, i32, vp, i32, vp, i32, i32, f32, vp, i32, vp, ctypes.c_size_t, vp]),
         "pa_decode_split_static": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp]),
         "pa_copy_blocks": (i32, [vp, vp, vp, i32, vp]),
         "pa_check": (i32, [vp, vp, ctypes.POINTER(i64)]),
@@ -241,6 +243,28 @@ def pa_append_decode(pool, q, k_new, v_new, block_tables, seq_lens, scale, out, 
                                 int(partition_blocks), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "pa_append_decode")
+
+
+def pa_decode_multi(pool, q, q_start, block_tables, seq_lens, scale, out, workspace=None, stream=None):
+    """Several new query tokens per sequence (causal within them); q and out
+    are [n_q][Hq][128], q_start int32 [B+1] on the device (see include/pa.h)."""
+    _need(q, "q", pool.dtype); _need(q_start, "q_start", torch.int32)
+    _need(block_tables, "block_tables", torch.int32); _need(seq_lens, "seq_lens", torch.int32); _need(out, "out")
+    n_q, Hq, d = q.shape
+    B = seq_lens.shape[0]
+    if d != HEAD_DIM or q_start.shape != (B + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("shapes: q [n_q][Hq][128], q_start [B+1], block_tables [B][W], seq_lens [B]")
+    if out.shape != q.shape or out.dtype not in _DTYPE_CODE:
+        raise ValueError("out must be [n_q][Hq][128] of fp16, bf16 or fp32")
+    W = block_tables.shape[1]
+    if workspace is None:
+        n = lib.pa_decode_multi_workspace_bytes(pool.handle, n_q, Hq, W)
+        if n == 0:
+            raise PagedAttentionError(PA_ERR_INVALID, "pa_decode_multi_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(lib.pa_decode_multi(pool.handle, _ptr(q), _ptr(q_start), n_q, _ptr(block_tables), W, _ptr(seq_lens), B, Hq,
+                               float(scale), _ptr(out), _DTYPE_CODE[out.dtype], _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "pa_decode_multi")
 
 
 def pa_copy_blocks(pool, src, dst, stream=None):

@@ -81,7 +81,8 @@ struct Params {
   const uint16_t* v_pool;
   const uint16_t* k_new;    // [B][Hkv][128], fused append only
   const uint16_t* v_new;
-  const int32_t* tables;    // [B][max_blocks]
+  const int32_t* tables;    // [rows][max_blocks]
+  const int32_t* table_rows;  // [B]: table row of sequence i, or null (row i)
   const int32_t* seq_lens;  // [B]
   void* out;                // [B][Hq][128]
   float* ws;                // partial records
@@ -445,7 +446,7 @@ struct SegmentRecords {
 // LEAN, partitions for PARTITION) into pfx[0..B], and, when lens is given, the
 // clamped lengths into lens[0..B).  All threads of the block load the
 // lengths; warp 0 scans.  Ends with a block barrier.
-__device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report) {
+__device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report, int* rows = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cap = P.max_blocks * kBlock;
   for (int i = threadIdx.x; i < P.B; i += blockDim.x) {
@@ -455,6 +456,7 @@ __device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report) 
       L = L < 0 ? 0 : cap;
     }
     if (lens) lens[i] = L;
+    if (rows) rows[i] = P.table_rows[i];
     const int nb = (L + kBlock - 1) / kBlock;
     pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
   }
@@ -508,8 +510,8 @@ static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() 
 // Dynamic shared memory to request: the struct, the prefix array, and slack
 // to align the base to 1024 bytes.
 template <int G>
-constexpr size_t smem_bytes(int B) {
-  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>(2 * B + 1) + 1024;
+constexpr size_t smem_bytes(int B, bool rows = false) {
+  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>((rows ? 3 : 2) * B + 1) + 1024;
 }
 
 // ---------------------------------------------------------------------------
@@ -534,7 +536,9 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0);
+  // tail of shared memory: prefix [B+1], lengths [B], table rows [B] (when given)
+  int* const S_rows = P.table_rows ? S.pfx + 2 * P.B + 1 : nullptr;
+  if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0, S_rows);
   // the merge kernel that follows may start its own set-up now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -587,7 +591,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   int n_issued = 0;
   auto window = [&](const Piece& pp, int base) -> int {
     const int jj = base + lane;
-    return jj < pp.j1 ? P.tables[static_cast<long long>(pp.i) * P.max_blocks + jj] : 0;
+    const long long row = S_rows ? S_rows[pp.i] : pp.i;
+    return jj < pp.j1 ? P.tables[row * P.max_blocks + jj] : 0;
   };
   auto prefetch_rows = [&](const Piece& pp) {
     const long long qrow = (static_cast<long long>(pp.i) * P.Hq + pp.h * G) * kHeadDim;
@@ -1113,6 +1118,34 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+// Several new query tokens per sequence: each query row becomes its own
+// (virtual) sequence that reads its owner's table row over the causal prefix
+// it may see.  Row r of sequence i (q_start[i] <= r < q_start[i+1], T_i rows)
+// sits at position L_i - T_i + (r - q_start[i]) and attends over that many
+// tokens plus one.
+// ---------------------------------------------------------------------------
+__global__ void multi_prep_kernel(const int32_t* __restrict__ q_start, const int32_t* __restrict__ seq_lens,
+                                  int B, int n_q, int cap, int32_t* __restrict__ lens_out,
+                                  int32_t* __restrict__ rows_out, long long* err) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_q) return;
+  int lo = 0, hi = B - 1;  // the last i with q_start[i] <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (q_start[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  const int T = q_start[lo + 1] - q_start[lo];
+  int L = seq_lens[lo];
+  int len = L - T + (r - q_start[lo]) + 1;
+  if (L < 0 || L > cap || T <= 0 || len < 1 || len > L) {
+    record_error(err, PA_ERR_DEVICE_CHECK, static_cast<long long>(r));
+    len = 0;  // an all-zero output row
+  }
+  lens_out[r] = len;
+  rows_out[r] = lo;
+}
+
+// ---------------------------------------------------------------------------
 // Host side: dispatch over (G, dtype, fused).
 // ---------------------------------------------------------------------------
 
@@ -1138,7 +1171,7 @@ static int occupancy_for(size_t bytes) {
   if (dev == cached_dev && bytes == cached_bytes) return cached_occ;
   if (cudaFuncSetAttribute(decode_kernel<G, kBf16, kFused>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_bytes<G>(kMaxSplitSeqs))) != cudaSuccess)
+                           static_cast<int>(smem_bytes<G>(kMaxSplitSeqs, true))) != cudaSuccess)
     return 0;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G, kBf16, kFused>,
@@ -1155,7 +1188,7 @@ template <int G, bool kBf16, bool kFused>
 static int launch_typed(Params& P, int device, cudaStream_t stream) {
   constexpr int NW = Shape<G>::NW;
   int B_smem = P.sched == SCHED_SEGMENT ? 0 : P.B;
-  size_t bytes = smem_bytes<G>(B_smem);
+  size_t bytes = smem_bytes<G>(B_smem, P.table_rows != nullptr);
   int occ = occupancy_for<G, kBf16, kFused>(bytes);
   if (occ <= 0) return PA_ERR_CUDA;
   long long slots = static_cast<long long>(sm_count(device)) * occ;
@@ -1245,7 +1278,8 @@ static bool workspace_layout(const pa_pool* p, int B, int Hq, int max_blocks, in
 static int decode_common(pa_pool_t p, const void* q, const void* k_new, const void* v_new,
                          const int32_t* tables, int max_blocks, const int32_t* seq_lens, int B,
                          int Hq, float scale, void* out, int out_dtype, int sched,
-                         int partition_blocks, void* ws, size_t ws_bytes, void* stream) {
+                         int partition_blocks, void* ws, size_t ws_bytes, void* stream,
+                         const int32_t* table_rows = nullptr) {
   if (!p || !q || !tables || !seq_lens || !out || B <= 0 || Hq <= 0 || max_blocks <= 0)
     return PA_ERR_INVALID;
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
@@ -1256,6 +1290,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   const bool fused = k_new != nullptr;
   if (fused && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15))
     return PA_ERR_INVALID;
+  if (table_rows && (sched == SCHED_SEGMENT || fused)) return PA_ERR_INVALID;
   WorkspaceLayout lay{};
   if (sched != SCHED_SEGMENT) {
     if (B > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
@@ -1270,6 +1305,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.k_new = static_cast<const uint16_t*>(k_new);
   P.v_new = static_cast<const uint16_t*>(v_new);
   P.tables = tables;
+  P.table_rows = table_rows;
   P.seq_lens = seq_lens;
   P.out = out;
   P.ws = static_cast<float*>(ws);
@@ -1360,6 +1396,41 @@ int pa_append_decode(pa_pool_t p, const void* q, const void* k_new, const void* 
   return decode_common(p, q, k_new, v_new, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        n_q_heads, scale, out, out_dtype, sched, partition_blocks, workspace,
                        workspace_bytes, stream);
+}
+
+// Multi-token queries: workspace = per-row lengths and table rows (int32
+// each, 256-byte aligned), then the balanced split's partial records.
+static size_t multi_head_bytes(int n_q) {
+  return (sizeof(int32_t) * 2 * static_cast<size_t>(n_q) + 255) / 256 * 256;
+}
+
+size_t pa_decode_multi_workspace_bytes(pa_pool_t p, int n_q, int n_q_heads, int max_blocks_per_seq) {
+  WorkspaceLayout lay{};
+  if (!p || n_q <= 0 || !workspace_layout(p, n_q, n_q_heads, max_blocks_per_seq, 0, &lay)) return 0;
+  return multi_head_bytes(n_q) + lay.total;
+}
+
+int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                    int num_seqs, int n_q_heads, float scale, void* out, int out_dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p || !q_start || !seq_lens || !block_tables || num_seqs <= 0 || n_q <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID;
+  if (n_q > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
+  const size_t need = pa_decode_multi_workspace_bytes(p, n_q, n_q_heads, max_blocks_per_seq);
+  if (need == 0) return PA_ERR_INVALID;
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return PA_ERR_INVALID;
+  int32_t* lens = static_cast<int32_t*>(workspace);
+  int32_t* rows = lens + n_q;
+  cudaStream_t st = as_stream(stream);
+  multi_prep_kernel<<<(n_q + 255) / 256, 256, 0, st>>>(q_start, seq_lens, num_seqs, n_q, max_blocks_per_seq * kBlock,
+                                                       lens, rows, p->err);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  const size_t head = multi_head_bytes(n_q);
+  return decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, lens, n_q, n_q_heads, scale, out,
+                       out_dtype, SCHED_LEAN, 0, static_cast<char*>(workspace) + head, workspace_bytes - head,
+                       stream, rows);
 }
 
 // ---------------------------------------------------------------------------
