@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--row", default="decode", choices=["decode", "multi-query", "prefix-cache", "utilisation"],
+                    help="decode: the headline step; the others time the further rows (one JSON line each)")
+    ap.add_argument("--new-tokens", type=int, default=4, help="multi-query: new tokens per sequence")
     return ap.parse_args()
 
 
@@ -346,6 +349,10 @@ def main():
                                              if backend == "nccl" else None)
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.row != "decode":
+        if rank == 0:
+            print(json.dumps(ROWS[args.row](args)), flush=True)
+        return
     r = run_ours(args, rank, world, local)
     cfg, nb = r["cfg"], r["nbytes"]
     peak, peak_kind = measured_peak()
@@ -415,6 +422,111 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_multi_query(args):
+    """Several new tokens per sequence (speculative verification shape) on the
+    workload's sequences: pa_decode_multi, L2 flushed before each call.
+    Algorithmic bytes: each sequence's K/V once, plus q and out."""
+    import paged_kv_cache_227_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    pa_, cfg, case, tables, slots, dec_lens = build_inputs(args.workload, 0, device)
+    T = args.new_tokens
+    news = np.minimum(dec_lens, T).astype(np.int32)
+    q_start = np.concatenate([[0], np.cumsum(news)]).astype(np.int32)
+    n_q = int(q_start[-1])
+    pool = pa.Pool(case.num_blocks, cfg.n_kv_heads, cfg.torch_dtype)
+    pool.k.copy_(case.k_pool.to(device))
+    pool.v.copy_(case.v_pool.to(device))
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(n_q, cfg.n_q_heads, cfg.d_head, generator=g).to(cfg.torch_dtype).to(device)
+    out = torch.empty_like(q)
+    qs, bt, sl = (torch.from_numpy(x).to(device) for x in (q_start, tables, dec_lens))
+    ws = torch.empty(pa.lib.pa_decode_multi_workspace_bytes(pool.handle, n_q, cfg.n_q_heads, tables.shape[1]),
+                     dtype=torch.uint8, device=device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+    sink = torch.zeros(1, device=device)
+    K = max(1, min(args.steps, 2000))
+    for _ in range(max(args.warmup, 3)):
+        sink.add_(flush_buf.sum())
+        pa.pa_decode_multi(pool, q, qs, bt, sl, case.scale, out, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        sink.add_(flush_buf.sum())
+        ev[k][0].record()
+        pa.pa_decode_multi(pool, q, qs, bt, sl, case.scale, out, workspace=ws)
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    code, detail = pa.pa_check(pool)
+    assert code == 0, (pa.strerror(code), detail)
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    kv = int(np.sum(dec_lens)) * cfg.n_kv_heads * cfg.d_head * 2 * 2
+    nbytes = kv + 2 * n_q * cfg.n_q_heads * cfg.d_head * 2
+    peak, _ = measured_peak()
+    return {"row": "multi-query", "metric": "paged attention, several new tokens per sequence: GB/s",
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+            "frac_of_copy_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "steps": K,
+            "config": {"workload": cfg.name, "new_tokens_per_sequence": T, "query_rows": n_q,
+                       "bytes": nbytes, "l2": "flushed before every call"}}
+
+
+def run_prefix_cache(args):
+    """Host allocator: 2,048-token prompts found whole in the prefix cache
+    (128 block hashes each) and token-tracked appends."""
+    import paged_kv_cache_227_gb300 as pa
+    a = pa.BlockAllocator(4096)
+    prompt = (np.arange(2048) * 7919 % 50021).astype(np.int32)
+    a.seq_add_cached(0, [])
+    for t in prompt:
+        a.append_token(0, int(t))
+    a.seq_free(0)
+    n = 200
+    t0 = time.perf_counter()
+    for s in range(1, n + 1):
+        assert a.seq_add_cached(s, prompt) == 2048
+        a.seq_free(s)
+    dt_lookup = time.perf_counter() - t0
+    a.seq_add_cached(n + 1, [])
+    t0 = time.perf_counter()
+    for k in range(20000):
+        a.append_token(n + 1, k)
+    dt_append = time.perf_counter() - t0
+    return {"row": "prefix-cache", "metric": "prefix-cache lookups: cached blocks found per second (host)",
+            "value": round(n * 128 / dt_lookup, 1), "unit": "blocks/s",
+            "appends_per_s": round(20000 / dt_append, 1),
+            "config": {"prompt_tokens": 2048, "prompts": n, "note": "through the Python binding (one call per prompt)"}}
+
+
+def run_utilisation(args):
+    """Worst-case contiguous reservation vs paging on the 96-block demo and a
+    lognormal request stream (host replay)."""
+    from paged_kv_cache_227_gb300 import utilization as u
+    res = {}
+    t0 = time.perf_counter()
+    for pol in ("reserve", "paged"):
+        tr, adm = u.run(pol, 96, u.demo_requests(), 700)
+        res[f"demo_{pol}"] = {"max_running": max(s.running for s in tr), "utilisation": round(u.utilisation(tr), 4),
+                              "admitted_at": adm}
+    rng = np.random.default_rng(0)
+    n = 60
+    arr = np.sort(rng.integers(0, 400, n))
+    pr = np.clip(np.round(np.exp(np.log(150) + 0.9 * rng.standard_normal(n))), 1, 2000).astype(int)
+    outp = np.clip(np.round(np.exp(np.log(200) + 0.8 * rng.standard_normal(n))), 1, 2000).astype(int)
+    reqs = [(int(a_), int(p_), int(o_), 2048) for a_, p_, o_ in zip(arr, pr, outp)]
+    for pol in ("reserve", "paged"):
+        tr, adm = u.run(pol, 1024, reqs, 1500)
+        res[f"lognormal_{pol}"] = {"max_running": max(s.running for s in tr),
+                                   "utilisation": round(u.utilisation(tr), 4)}
+    dt = time.perf_counter() - t0
+    return {"row": "utilisation", "metric": "token slots holding tokens / slots held (paged)",
+            "value": res["lognormal_paged"]["utilisation"], "unit": "fraction", "results": res,
+            "seconds": round(dt, 3)}
+
+
+ROWS = {"multi-query": run_multi_query, "prefix-cache": run_prefix_cache, "utilisation": run_utilisation}
 
 
 def run_reference(args, rank, world):

@@ -120,6 +120,15 @@ def run(policy, num_blocks, requests, steps, block_size=BLOCK_SIZE):
     return out, admitted
 
 
+def demo_requests():
+    """The 96-block, eight-request demo as this library reads it: a request may
+    grow to 384 tokens (24 blocks, so four reservations fill the pool) and
+    holds at most 170; one arrives every 10 steps."""
+    prompts = [30, 45, 20, 60, 35, 50, 25, 40]
+    outputs = [120, 90, 150, 60, 100, 80, 130, 70]
+    return [Request(10 * k, p, o, 384) for k, (p, o) in enumerate(zip(prompts, outputs))]
+
+
 def utilisation(trace, block_size=BLOCK_SIZE):
     """Tokens held over token slots held, over the steps where anything runs."""
     held = sum(s.blocks for s in trace) * block_size

@@ -20,6 +20,10 @@ def same(trace, ref_trace):
         [(s["step"], s["running"], s["blocks"], s["tokens"], s["admitted"]) for s in ref_trace]
 
 
+def test_demo_schedule_is_the_references(util):
+    assert [(r.arrival, r.prompt, r.output, r.max_tokens) for r in util.demo_requests()] == demo_requests()
+
+
 @pytest.mark.parametrize("policy", ["reserve", "paged"])
 def test_demo_matches_reference(util, policy):
     reqs = demo_requests()
