@@ -202,6 +202,30 @@ int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n
                     float scale, void* out, int out_dtype, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* Shared-prefix (cascade) decode: pa_decode's result, with each group's
+ * shared prefix read once for all of its members ("Serving" 23.4: sequences
+ * that share a prefix share its blocks).  Group k's members are
+ * members[group_start[k] .. group_start[k+1]-1] (device int32; 2 to
+ * floor(8 / (n_q_heads / n_kv_heads)) sequences); they share their first
+ * prefix_blocks[k] table entries (the same physical blocks), each full
+ * (16 * prefix_blocks[k] <= every member's length).  One pass attends every
+ * member's query heads over the shared blocks as one segment per (group, kv
+ * head); a second attends each sequence over its blocks after its group's
+ * prefix (all of them for a sequence in no group); a third merges the two by
+ * log-sum-exp.  A group that breaks these rules is reported
+ * (PA_ERR_DEVICE_CHECK) and its members are decoded without it.  q, out,
+ * block_tables, seq_lens as for pa_decode; num_seqs and n_groups <= 4096.
+ * workspace: device, >= pa_decode_cascade_workspace_bytes(...), 256-byte
+ * aligned. */
+size_t pa_decode_cascade_workspace_bytes(pa_pool_t pool, int num_seqs, int n_q_heads,
+                                         int max_blocks_per_seq, int n_groups);
+int pa_decode_cascade(pa_pool_t pool, const void* q, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                      int n_q_heads, float scale, const int32_t* group_start,
+                      const int32_t* members, const int32_t* prefix_blocks, int n_groups,
+                      void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
 /* Split-KV decode that allocates nothing (the pages have no counterpart; this
  * is a deployment convenience).  Some callers cannot call cudaMalloc at the
  * time they decode: a serving loop whose device memory budget is fixed up
@@ -309,6 +333,16 @@ int pa_alloc_seq_len(pa_alloc_t a, int seq);
 int pa_alloc_refcount(pa_alloc_t a, int block);
 /* Number of blocks on the free list. */
 int pa_alloc_num_free(pa_alloc_t a);
+/* Groups for pa_decode_cascade from host block tables: sequences whose
+ * first blocks are the same, in order of first appearance, cut into groups
+ * of at most max_members; a group's prefix is the run of table entries all
+ * its members share, counting only blocks full in every member; groups of one
+ * or with no shared full block are dropped.  Outputs (host, capacity
+ * num_seqs + 1, num_seqs, num_seqs): group_start, members, prefix_blocks;
+ * *n_groups receives the count. */
+int pa_cascade_groups(const int32_t* tables, int num_seqs, int max_blocks,
+                      const int32_t* seq_lens, int max_members, int32_t* group_start,
+                      int32_t* members, int32_t* prefix_blocks, int* n_groups);
 
 /* ---------------------------------------------------------------------------
  * Prefix caching by block hashes ("Paged Attention" teaser on the

@@ -53,6 +53,10 @@ def _load():
         "pa_append_decode": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
         "pa_decode_multi_workspace_bytes": (ctypes.c_size_t, [vp, i32, i32, i32]),
         "pa_decode_multi": (i32, [vp, vp, vp, i32, vp, i32, vp, i32, i32, f32, vp, i32, vp, ctypes.c_size_t, vp]),
+        "pa_decode_cascade_workspace_bytes": (ctypes.c_size_t, [vp, i32, i32, i32, i32]),
+        "pa_decode_cascade": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, vp, vp, i32, vp, i32, vp,
+                                    ctypes.c_size_t, vp]),
+        "pa_cascade_groups": (i32, [vp, i32, i32, vp, i32, vp, vp, vp, ctypes.POINTER(i32)]),
         "pa_decode_split_static": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp]),
         "pa_copy_blocks": (i32, [vp, vp, vp, i32, vp]),
         "pa_check": (i32, [vp, vp, ctypes.POINTER(i64)]),
@@ -265,6 +269,45 @@ def pa_decode_multi(pool, q, q_start, block_tables, seq_lens, scale, out, worksp
     _check(lib.pa_decode_multi(pool.handle, _ptr(q), _ptr(q_start), n_q, _ptr(block_tables), W, _ptr(seq_lens), B, Hq,
                                float(scale), _ptr(out), _DTYPE_CODE[out.dtype], _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)), "pa_decode_multi")
+
+
+def cascade_groups(block_tables, seq_lens, n_q_heads, n_kv_heads):
+    """Host: (group_start, members, prefix_blocks) int32 numpy arrays for
+    pa_decode_cascade from host tables [B][W] and lengths [B]."""
+    import numpy as np
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, W = t.shape
+    gs = np.zeros(B + 1, np.int32)
+    mem = np.zeros(max(B, 1), np.int32)
+    pre = np.zeros(max(B, 1), np.int32)
+    ng = ctypes.c_int()
+    _check(lib.pa_cascade_groups(t.ctypes.data_as(ctypes.c_void_p), B, W, lens.ctypes.data_as(ctypes.c_void_p),
+                                 MAX_GROUP // (n_q_heads // n_kv_heads), gs.ctypes.data_as(ctypes.c_void_p),
+                                 mem.ctypes.data_as(ctypes.c_void_p), pre.ctypes.data_as(ctypes.c_void_p),
+                                 ctypes.byref(ng)), "pa_cascade_groups")
+    n = ng.value
+    return gs[:n + 1].copy(), mem[:gs[n]].copy(), pre[:n].copy()
+
+
+def pa_decode_cascade(pool, q, block_tables, seq_lens, scale, out, group_start, members, prefix_blocks,
+                      workspace=None, stream=None):
+    """pa_decode with each group's shared prefix read once (include/pa.h);
+    the group arrays are int32 device tensors."""
+    B, Hq, W = _decode_args(pool, q, block_tables, seq_lens, out)
+    for t, n in ((group_start, "group_start"), (members, "members"), (prefix_blocks, "prefix_blocks")):
+        _need(t, n, torch.int32)
+    ng = prefix_blocks.shape[0]
+    if workspace is None:
+        n = lib.pa_decode_cascade_workspace_bytes(pool.handle, B, Hq, W, ng)
+        if n == 0:
+            raise PagedAttentionError(PA_ERR_INVALID, "pa_decode_cascade_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(lib.pa_decode_cascade(pool.handle, _ptr(q), _ptr(block_tables), W, _ptr(seq_lens), B, Hq, float(scale),
+                                 _ptr(group_start) if ng else None, _ptr(members) if ng else None,
+                                 _ptr(prefix_blocks) if ng else None, ng, _ptr(out), _DTYPE_CODE[out.dtype],
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "pa_decode_cascade")
 
 
 def pa_copy_blocks(pool, src, dst, stream=None):

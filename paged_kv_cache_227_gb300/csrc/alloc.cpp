@@ -8,6 +8,7 @@
 // by the chained hash of their tokens (prefix caching by block hashes, same
 // page; hash chains, posts on the pagedattention tag).  The policy is spelled
 // out in pa.h.
+#include <algorithm>
 #include <array>
 #include <cstring>
 #include <list>
@@ -307,6 +308,54 @@ int pa_alloc_seq_len(pa_alloc_t a, int seq) {
 int pa_alloc_refcount(pa_alloc_t a, int block) {
   if (!a || block < 0 || block >= a->num_blocks) return PA_ERR_INVALID;
   return a->refcount[block];
+}
+
+int pa_cascade_groups(const int32_t* tables, int num_seqs, int max_blocks, const int32_t* seq_lens,
+                      int max_members, int32_t* group_start, int32_t* members, int32_t* prefix_blocks,
+                      int* n_groups) {
+  if (!tables || !seq_lens || !group_start || !members || !prefix_blocks || !n_groups || num_seqs < 0 ||
+      max_blocks <= 0 || max_members < 1)
+    return PA_ERR_INVALID;
+  // sequences by first block, in order of first appearance
+  std::vector<int32_t> keys;
+  std::unordered_map<int32_t, std::vector<int>> by_first;
+  for (int i = 0; i < num_seqs; ++i) {
+    if (seq_lens[i] < 16) continue;  // no full block to share
+    const int32_t b = tables[static_cast<long long>(i) * max_blocks];
+    auto it = by_first.find(b);
+    if (it == by_first.end()) {
+      keys.push_back(b);
+      by_first.emplace(b, std::vector<int>{i});
+    } else {
+      it->second.push_back(i);
+    }
+  }
+  int ng = 0, nm = 0;
+  group_start[0] = 0;
+  for (int32_t b : keys) {
+    const std::vector<int>& all = by_first[b];
+    for (size_t c0 = 0; c0 < all.size(); c0 += static_cast<size_t>(max_members)) {
+      const size_t c1 = std::min(all.size(), c0 + static_cast<size_t>(max_members));
+      if (c1 - c0 < 2) continue;
+      int lim = max_blocks;
+      for (size_t k = c0; k < c1; ++k) lim = std::min(lim, seq_lens[all[k]] / 16);
+      const int32_t* t0 = tables + static_cast<long long>(all[c0]) * max_blocks;
+      int P = 0;
+      while (P < lim) {
+        bool same = true;
+        for (size_t k = c0 + 1; k < c1 && same; ++k)
+          same = tables[static_cast<long long>(all[k]) * max_blocks + P] == t0[P];
+        if (!same) break;
+        ++P;
+      }
+      if (P < 1) continue;
+      for (size_t k = c0; k < c1; ++k) members[nm++] = all[k];
+      prefix_blocks[ng] = P;
+      group_start[++ng] = nm;
+    }
+  }
+  *n_groups = ng;
+  return PA_OK;
 }
 
 int pa_alloc_num_free(pa_alloc_t a) {

@@ -82,7 +82,8 @@ struct Params {
   const uint16_t* k_new;    // [B][Hkv][128], fused append only
   const uint16_t* v_new;
   const int32_t* tables;    // [rows][max_blocks]
-  const int32_t* table_rows;  // [B]: table row of sequence i, or null (row i)
+  const int32_t* table_offs;  // [B]: element offset of sequence i's table row, or null (i * max_blocks)
+  float* lse;               // [B][Hq] log2-sum-exp of the scaled scores (log2 units), or null
   const int32_t* seq_lens;  // [B]
   void* out;                // [B][Hq][128]
   float* ws;                // partial records
@@ -456,7 +457,7 @@ __device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report, 
       L = L < 0 ? 0 : cap;
     }
     if (lens) lens[i] = L;
-    if (rows) rows[i] = P.table_rows[i];
+    if (rows) rows[i] = P.table_offs[i];
     const int nb = (L + kBlock - 1) / kBlock;
     pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
   }
@@ -536,8 +537,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // tail of shared memory: prefix [B+1], lengths [B], table rows [B] (when given)
-  int* const S_rows = P.table_rows ? S.pfx + 2 * P.B + 1 : nullptr;
+  // tail of shared memory: prefix [B+1], lengths [B], table offsets [B] (when given)
+  int* const S_rows = P.table_offs ? S.pfx + 2 * P.B + 1 : nullptr;
   if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0, S_rows);
   // the merge kernel that follows may start its own set-up now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -548,6 +549,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       if (S.pfx[i + 1] != S.pfx[i]) continue;
       for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x)
         store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
+      if (P.lse)
+        for (int x = threadIdx.x; x < P.Hq; x += blockDim.x) P.lse[static_cast<long long>(i) * P.Hq + x] = -INFINITY;
     }
   }
 
@@ -591,8 +594,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   int n_issued = 0;
   auto window = [&](const Piece& pp, int base) -> int {
     const int jj = base + lane;
-    const long long row = S_rows ? S_rows[pp.i] : pp.i;
-    return jj < pp.j1 ? P.tables[row * P.max_blocks + jj] : 0;
+    const long long off = S_rows ? S_rows[pp.i] : static_cast<long long>(pp.i) * P.max_blocks;
+    return jj < pp.j1 ? P.tables[off + jj] : 0;
   };
   auto prefetch_rows = [&](const Piece& pp) {
     const long long qrow = (static_cast<long long>(pp.i) * P.Hq + pp.h * G) * kHeadDim;
@@ -943,6 +946,11 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     }
     const long long row0 = (static_cast<long long>(pc.i) * P.Hq + pc.h * G) * kHeadDim;
     float* rec = P.ws + pc.rec * record_floats(G);
+    if (pc.final_out && P.lse && lane == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        P.lse[static_cast<long long>(pc.i) * P.Hq + pc.h * G + g] = lg[g] > 0.f ? mg[g] + __log2f(lg[g]) : -INFINITY;
+    }
     if constexpr (kMmaPv) {
       // o = high + low columns; lanes c4 and c4^2 then hold the same sums:
       // lane c4 < 2 writes dims 16mt+r4, lane c4 >= 2 dims 16mt+r4+8, of
@@ -1114,6 +1122,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
     const long long idx = (static_cast<long long>(i) * P.Hq + h * G + g) * kHeadDim + 4 * lane;
     store_out4(P.out, idx, O.x * inv, O.y * inv, O.z * inv, O.w * inv, P.out_dtype);
+    if (P.lse && lane == 0)
+      P.lse[static_cast<long long>(i) * P.Hq + h * G + g] = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
   }
 }
 
@@ -1142,7 +1152,142 @@ __global__ void multi_prep_kernel(const int32_t* __restrict__ q_start, const int
     len = 0;  // an all-zero output row
   }
   lens_out[r] = len;
-  rows_out[r] = lo;
+  rows_out[r] = lo * (cap / kBlock);  // element offset of the owner's table row
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix (cascade) decode.  The members of group k share their first
+// P_k blocks (the same physical blocks at the start of their tables).  The
+// prefix pass attends all members' queries over those blocks in one segment
+// per (group, kv head): member m's G query heads become columns m*G..m*G+G-1
+// of a group of SM*G columns (SM = floor(8 / G) members at most), so each
+// shared tile is read once for every member.  The suffix pass attends each
+// sequence over its own blocks after the prefix.  Both passes return the
+// normalised output and the log2-sum-exp; the combine kernel merges them.
+// ---------------------------------------------------------------------------
+struct CascadeArgs {
+  const uint16_t* q;              // [B][Hq][128]
+  const int32_t* seq_lens;        // [B]
+  const int32_t* tables;          // [B][max_blocks]
+  const int32_t* group_start;     // [n_groups + 1]
+  const int32_t* members;         // [group_start[n_groups]]
+  const int32_t* prefix_blocks;   // [n_groups]
+  int B, Hq, Hkv, G, SM, n_groups, max_blocks;
+  // workspace
+  uint16_t* qv;                   // [n_groups][Hkv*SM*G][128]
+  int32_t* lens_v;                // [n_groups]
+  int32_t* offs_v;                // [n_groups]
+  int32_t* lens_s;                // [B]
+  int32_t* offs_s;                // [B]
+  int32_t* slot_of;               // [B]: group * 8 + member slot, or -1
+  long long* err;
+};
+
+// One CTA per group: member slots, prefix lengths and offsets, and the
+// packed queries of the prefix pass (zero past the group's members).
+__global__ void cascade_prep_groups(CascadeArgs A) {
+  __shared__ int s_bad;
+  const int k = blockIdx.x;
+  const int m0 = A.group_start[k], m1 = A.group_start[k + 1];
+  const int S = m1 - m0;
+  const int P = A.prefix_blocks[k];
+  const int cap = A.max_blocks * kBlock;
+  if (threadIdx.x == 0) {
+    bool bad = S < 1 || S > A.SM || P < 0 || P > A.max_blocks;
+    for (int m = 0; !bad && m < S; ++m) {
+      const int i = A.members[m0 + m];
+      bad = i < 0 || i >= A.B || A.seq_lens[i] < P * kBlock || A.seq_lens[i] > cap;
+    }
+    s_bad = bad;
+  }
+  __syncthreads();
+  if (!s_bad) {  // the shared blocks must be the first member's
+    const int first = A.members[m0];
+    for (int x = threadIdx.x; x < S * P; x += blockDim.x) {
+      const int i = A.members[m0 + x / P];
+      if (A.tables[static_cast<long long>(i) * A.max_blocks + x % P] !=
+          A.tables[static_cast<long long>(first) * A.max_blocks + x % P])
+        s_bad = 1;
+    }
+  }
+  __syncthreads();
+  if (s_bad) {  // reported; its members are decoded without the group
+    if (threadIdx.x == 0) {
+      record_error(A.err, PA_ERR_DEVICE_CHECK, k);
+      A.lens_v[k] = 0;
+      A.offs_v[k] = 0;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    A.lens_v[k] = P * kBlock;
+    A.offs_v[k] = A.members[m0] * A.max_blocks;
+  }
+  for (int m = threadIdx.x; m < S; m += blockDim.x) A.slot_of[A.members[m0 + m]] = k * 8 + m;
+  // packed queries: 16-byte vectors
+  const int GC = A.SM * A.G;  // columns per kv head
+  const long long n_vec = static_cast<long long>(A.Hkv) * GC * (kHeadDim / 8);
+  const uint4* q = reinterpret_cast<const uint4*>(A.q);
+  uint4* qv = reinterpret_cast<uint4*>(A.qv) + static_cast<long long>(k) * n_vec;
+  for (long long x = threadIdx.x; x < n_vec; x += blockDim.x) {
+    const int c = static_cast<int>(x / (kHeadDim / 8));
+    const int h = c / GC, col = c % GC, m = col / A.G, g = col % A.G;
+    const int w = static_cast<int>(x % (kHeadDim / 8));
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < S) {
+      const int i = A.members[m0 + m];
+      v = q[((static_cast<long long>(i) * A.Hq + h * A.G + g) * kHeadDim) / 8 + w];
+    }
+    qv[x] = v;
+  }
+}
+
+// One thread per sequence: its suffix after its group's prefix (all of it
+// when it is in no group).  Runs after cascade_prep_groups.
+__global__ void cascade_prep_seqs(CascadeArgs A) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= A.B) return;
+  int L = A.seq_lens[i];
+  const int cap = A.max_blocks * kBlock;
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int slot = A.slot_of[i];
+  const int P = slot >= 0 ? A.prefix_blocks[slot >> 3] : 0;
+  const int start = P * kBlock <= L ? P : 0;
+  A.lens_s[i] = L - start * kBlock;
+  A.offs_s[i] = i * A.max_blocks + start;
+}
+
+// One warp per (sequence, query head): merge the two passes' normalised
+// outputs o1, o2 with log2-sum-exps e1, e2:
+//   out = (2^e1 o1 + 2^e2 o2) / (2^e1 + 2^e2).
+__global__ void cascade_combine(CascadeArgs A, const float* o_v, const float* lse_v, const float* o_s,
+                                const float* lse_s, void* out, int out_dtype) {
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<long long>(A.B) * A.Hq) return;
+  const int i = static_cast<int>(wid / A.Hq), hq = static_cast<int>(wid % A.Hq);
+  const float4 b = reinterpret_cast<const float4*>(o_s + wid * kHeadDim)[lane];
+  float e2 = lse_s[wid];
+  float4 r = b;
+  const int slot = A.slot_of[i];
+  if (slot >= 0) {
+    const int k = slot >> 3, m = slot & 7;
+    const int GC = A.SM * A.G;
+    const int h = hq / A.G, g = hq % A.G;
+    const long long row = static_cast<long long>(k) * A.Hkv * GC + h * GC + m * A.G + g;
+    const float4 a = reinterpret_cast<const float4*>(o_v + row * kHeadDim)[lane];
+    const float e1 = lse_v[row];
+    const float M = fmaxf(e1, e2);
+    if (M > -INFINITY) {
+      const float w1 = fast_exp2(e1 - M), w2 = fast_exp2(e2 - M);
+      const float inv = 1.f / (w1 + w2);
+      r = make_float4((w1 * a.x + w2 * b.x) * inv, (w1 * a.y + w2 * b.y) * inv, (w1 * a.z + w2 * b.z) * inv,
+                      (w1 * a.w + w2 * b.w) * inv);
+    } else {
+      r = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  store_out4(out, wid * kHeadDim + 4 * lane, r.x, r.y, r.z, r.w, out_dtype);
 }
 
 // ---------------------------------------------------------------------------
@@ -1188,7 +1333,7 @@ template <int G, bool kBf16, bool kFused>
 static int launch_typed(Params& P, int device, cudaStream_t stream) {
   constexpr int NW = Shape<G>::NW;
   int B_smem = P.sched == SCHED_SEGMENT ? 0 : P.B;
-  size_t bytes = smem_bytes<G>(B_smem, P.table_rows != nullptr);
+  size_t bytes = smem_bytes<G>(B_smem, P.table_offs != nullptr);
   int occ = occupancy_for<G, kBf16, kFused>(bytes);
   if (occ <= 0) return PA_ERR_CUDA;
   long long slots = static_cast<long long>(sm_count(device)) * occ;
@@ -1279,7 +1424,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
                          const int32_t* tables, int max_blocks, const int32_t* seq_lens, int B,
                          int Hq, float scale, void* out, int out_dtype, int sched,
                          int partition_blocks, void* ws, size_t ws_bytes, void* stream,
-                         const int32_t* table_rows = nullptr) {
+                         const int32_t* table_offs = nullptr, float* lse = nullptr) {
   if (!p || !q || !tables || !seq_lens || !out || B <= 0 || Hq <= 0 || max_blocks <= 0)
     return PA_ERR_INVALID;
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
@@ -1290,7 +1435,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   const bool fused = k_new != nullptr;
   if (fused && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15))
     return PA_ERR_INVALID;
-  if (table_rows && (sched == SCHED_SEGMENT || fused)) return PA_ERR_INVALID;
+  if ((table_offs || lse) && (sched == SCHED_SEGMENT || fused)) return PA_ERR_INVALID;
   WorkspaceLayout lay{};
   if (sched != SCHED_SEGMENT) {
     if (B > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
@@ -1305,7 +1450,8 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.k_new = static_cast<const uint16_t*>(k_new);
   P.v_new = static_cast<const uint16_t*>(v_new);
   P.tables = tables;
-  P.table_rows = table_rows;
+  P.table_offs = table_offs;
+  P.lse = lse;
   P.seq_lens = seq_lens;
   P.out = out;
   P.ws = static_cast<float*>(ws);
@@ -1431,6 +1577,111 @@ int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
   return decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, lens, n_q, n_q_heads, scale, out,
                        out_dtype, SCHED_LEAN, 0, static_cast<char*>(workspace) + head, workspace_bytes - head,
                        stream, rows);
+}
+
+// Shared-prefix decode: workspace pieces, each 256-byte aligned.
+struct CascadeLayout {
+  size_t qv, o_v, lse_v, lens_v, offs_v, o_s, lse_s, lens_s, offs_s, slot_of, rec, total;
+};
+static bool cascade_layout(const pa_pool* p, int B, int Hq, int max_blocks, int n_groups, CascadeLayout* L) {
+  if (!p || B <= 0 || Hq <= 0 || n_groups < 0 || max_blocks <= 0 || Hq % p->n_kv_heads) return false;
+  const int G = Hq / p->n_kv_heads;
+  if (G > PA_MAX_GROUP) return false;
+  const int GC = (PA_MAX_GROUP / G) * G;
+  const size_t rows_v = static_cast<size_t>(n_groups) * p->n_kv_heads * GC;
+  WorkspaceLayout ra{}, rb{};
+  if (n_groups > 0 && !workspace_layout(p, n_groups, p->n_kv_heads * GC, max_blocks, 0, &ra)) return false;
+  if (!workspace_layout(p, B, Hq, max_blocks, 0, &rb)) return false;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  L->qv = take(rows_v * kHeadDim * 2);
+  L->o_v = take(rows_v * kHeadDim * 4);
+  L->lse_v = take(rows_v * 4);
+  L->lens_v = take(static_cast<size_t>(n_groups) * 4);
+  L->offs_v = take(static_cast<size_t>(n_groups) * 4);
+  L->o_s = take(static_cast<size_t>(B) * Hq * kHeadDim * 4);
+  L->lse_s = take(static_cast<size_t>(B) * Hq * 4);
+  L->lens_s = take(static_cast<size_t>(B) * 4);
+  L->offs_s = take(static_cast<size_t>(B) * 4);
+  L->slot_of = take(static_cast<size_t>(B) * 4);
+  L->rec = take(ra.total > rb.total ? ra.total : rb.total);
+  L->total = off;
+  return true;
+}
+
+size_t pa_decode_cascade_workspace_bytes(pa_pool_t p, int num_seqs, int n_q_heads, int max_blocks_per_seq,
+                                         int n_groups) {
+  CascadeLayout L{};
+  return cascade_layout(p, num_seqs, n_q_heads, max_blocks_per_seq, n_groups, &L) ? L.total : 0;
+}
+
+int pa_decode_cascade(pa_pool_t p, const void* q, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* seq_lens, int num_seqs, int n_q_heads, float scale,
+                      const int32_t* group_start, const int32_t* members, const int32_t* prefix_blocks,
+                      int n_groups, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (!p || !q || !block_tables || !seq_lens || !out || num_seqs <= 0 || n_groups < 0 ||
+      (n_groups > 0 && (!group_start || !members || !prefix_blocks)))
+    return PA_ERR_INVALID;
+  if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
+  if (num_seqs > kMaxSplitSeqs || n_groups > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PA_ERR_INVALID;
+  CascadeLayout L{};
+  if (!cascade_layout(p, num_seqs, n_q_heads, max_blocks_per_seq, n_groups, &L)) return PA_ERR_INVALID;
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return PA_ERR_INVALID;
+  char* ws = static_cast<char*>(workspace);
+  const int G = n_q_heads / p->n_kv_heads;
+  CascadeArgs A{};
+  A.q = static_cast<const uint16_t*>(q);
+  A.seq_lens = seq_lens;
+  A.tables = block_tables;
+  A.group_start = group_start;
+  A.members = members;
+  A.prefix_blocks = prefix_blocks;
+  A.B = num_seqs;
+  A.Hq = n_q_heads;
+  A.Hkv = p->n_kv_heads;
+  A.G = G;
+  A.SM = PA_MAX_GROUP / G;
+  A.n_groups = n_groups;
+  A.max_blocks = max_blocks_per_seq;
+  A.qv = reinterpret_cast<uint16_t*>(ws + L.qv);
+  A.lens_v = reinterpret_cast<int32_t*>(ws + L.lens_v);
+  A.offs_v = reinterpret_cast<int32_t*>(ws + L.offs_v);
+  A.lens_s = reinterpret_cast<int32_t*>(ws + L.lens_s);
+  A.offs_s = reinterpret_cast<int32_t*>(ws + L.offs_s);
+  A.slot_of = reinterpret_cast<int32_t*>(ws + L.slot_of);
+  A.err = p->err;
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(A.slot_of, 0xff, sizeof(int32_t) * static_cast<size_t>(num_seqs), st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (n_groups > 0) cascade_prep_groups<<<n_groups, 256, 0, st>>>(A);
+  cascade_prep_seqs<<<(num_seqs + 255) / 256, 256, 0, st>>>(A);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  const size_t rec_bytes = L.total - L.rec;
+  float* o_v = reinterpret_cast<float*>(ws + L.o_v);
+  float* lse_v = reinterpret_cast<float*>(ws + L.lse_v);
+  float* o_s = reinterpret_cast<float*>(ws + L.o_s);
+  float* lse_s = reinterpret_cast<float*>(ws + L.lse_s);
+  int rc;
+  if (n_groups > 0) {
+    rc = decode_common(p, A.qv, nullptr, nullptr, block_tables, max_blocks_per_seq, A.lens_v, n_groups,
+                       p->n_kv_heads * A.SM * G, scale, o_v, PA_FP32, SCHED_LEAN, 0, ws + L.rec, rec_bytes, stream,
+                       A.offs_v, lse_v);
+    if (rc != PA_OK) return rc;
+  }
+  rc = decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, A.lens_s, num_seqs, n_q_heads, scale,
+                     o_s, PA_FP32, SCHED_LEAN, 0, ws + L.rec, rec_bytes, stream, A.offs_s, lse_s);
+  if (rc != PA_OK) return rc;
+  const long long warps = static_cast<long long>(num_seqs) * n_q_heads;
+  cascade_combine<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(A, o_v, lse_v, o_s, lse_s, out,
+                                                                                   out_dtype);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------
