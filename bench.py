@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--row", default="decode", choices=["decode", "multi-query", "prefix-cache", "utilisation"],
+    ap.add_argument("--row", default="decode",
+                    choices=["decode", "multi-query", "cascade", "prefix-cache", "utilisation"],
                     help="decode: the headline step; the others time the further rows (one JSON line each)")
     ap.add_argument("--new-tokens", type=int, default=4, help="multi-query: new tokens per sequence")
     return ap.parse_args()
@@ -473,6 +474,64 @@ def run_multi_query(args):
                        "bytes": nbytes, "l2": "flushed before every call"}}
 
 
+def run_cascade(args):
+    """Shared-prefix decode on the Llama-2-13B MHA workload (8 of 16 sequences
+    fork one 2,048-token prefix) against the plain balanced split on the same
+    inputs; L2 flushed before each call.  Bytes: unique K/V (the shared prefix
+    once) plus q and out, so plain decode is scored on the same numerator."""
+    import paged_kv_cache_227_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    _, cfg, case, tables, slots, dec_lens = build_inputs(4, 0, device)
+    pool = pa.Pool(case.num_blocks, cfg.n_kv_heads, cfg.torch_dtype)
+    pool.k.copy_(case.k_pool.to(device))
+    pool.v.copy_(case.v_pool.to(device))
+    q = case.q.to(device)
+    out = torch.empty_like(q)
+    bt, sl = torch.from_numpy(tables).to(device), torch.from_numpy(dec_lens).to(device)
+    gs, mem, pre = pa.cascade_groups(tables, dec_lens, cfg.n_q_heads, cfg.n_kv_heads)
+    gs_d, mem_d, pre_d = (torch.from_numpy(x).to(device) for x in (gs, mem, pre))
+    ws_c = torch.empty(pa.lib.pa_decode_cascade_workspace_bytes(pool.handle, len(dec_lens), cfg.n_q_heads,
+                                                                tables.shape[1], len(pre)),
+                       dtype=torch.uint8, device=device)
+    ws_s = pa.workspace_for(pool, q, bt, 0)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+    sink = torch.zeros(1, device=device)
+    calls = {"cascade": lambda: pa.pa_decode_cascade(pool, q, bt, sl, case.scale, out, gs_d, mem_d, pre_d,
+                                                     workspace=ws_c),
+             "split": lambda: pa.pa_decode_split(pool, q, bt, sl, case.scale, out, 0, ws_s)}
+    K = max(1, min(args.steps, 500))
+    res = {}
+    for name, fn in calls.items():
+        for _ in range(max(args.warmup, 3)):
+            sink.add_(flush_buf.sum())
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K):
+            sink.add_(flush_buf.sum())
+            ev[k][0].record()
+            fn()
+            ev[k][1].record()
+        torch.cuda.synchronize()
+        res[name] = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    code, detail = pa.pa_check(pool)
+    assert code == 0, (pa.strerror(code), detail)
+    tok_bytes = cfg.n_kv_heads * cfg.d_head * 2 * 2
+    unique = (int(np.sum(dec_lens)) - int(pre.astype(np.int64) @ (np.diff(gs) - 1)) * 16) * tok_bytes
+    nbytes = unique + 2 * q.numel() * 2
+    peak, _ = measured_peak()
+    return {"row": "cascade", "metric": "shared-prefix decode: unique bytes / time, GB/s",
+            "value": round(nbytes / (res["cascade"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "us_per_call": round(res["cascade"] * 1e3, 2),
+            "frac_of_copy_peak": round(nbytes / (res["cascade"] * 1e-3) / 1e9 / peak, 4),
+            "plain_split_us": round(res["split"] * 1e3, 2), "steps": K,
+            "config": {"workload": cfg.name, "groups": len(pre), "shared_prefix_blocks": pre.tolist(),
+                       "unique_bytes": nbytes, "logical_kv_bytes": int(np.sum(dec_lens)) * tok_bytes,
+                       "l2": "flushed before every call"}}
+
+
 def run_prefix_cache(args):
     """Host allocator: 2,048-token prompts found whole in the prefix cache
     (128 block hashes each) and token-tracked appends."""
@@ -526,7 +585,8 @@ def run_utilisation(args):
             "seconds": round(dt, 3)}
 
 
-ROWS = {"multi-query": run_multi_query, "prefix-cache": run_prefix_cache, "utilisation": run_utilisation}
+ROWS = {"multi-query": run_multi_query, "cascade": run_cascade, "prefix-cache": run_prefix_cache,
+        "utilisation": run_utilisation}
 
 
 def run_reference(args, rank, world):

@@ -518,7 +518,7 @@ constexpr size_t smem_bytes(int B, bool rows = false) {
 // ---------------------------------------------------------------------------
 // The decode kernel.
 // ---------------------------------------------------------------------------
-template <int G, bool kBf16, bool kFused>
+template <int G, bool kBf16, bool kFused, bool kExt>
 __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode_kernel(const __grid_constant__ Params P) {
   constexpr int NW = Shape<G>::NW;
   constexpr int SW = Shape<G>::SW;
@@ -537,8 +537,9 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // tail of shared memory: prefix [B+1], lengths [B], table offsets [B] (when given)
-  int* const S_rows = P.table_offs ? S.pfx + 2 * P.B + 1 : nullptr;
+  // tail of shared memory: prefix [B+1], lengths [B], table offsets [B]
+  // (kExt: per-sequence table offsets and log2-sum-exp outputs)
+  int* const S_rows = kExt ? S.pfx + 2 * P.B + 1 : nullptr;
   if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0, S_rows);
   // the merge kernel that follows may start its own set-up now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       if (S.pfx[i + 1] != S.pfx[i]) continue;
       for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x)
         store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
-      if (P.lse)
+      if (kExt && P.lse)
         for (int x = threadIdx.x; x < P.Hq; x += blockDim.x) P.lse[static_cast<long long>(i) * P.Hq + x] = -INFINITY;
     }
   }
@@ -594,7 +595,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   int n_issued = 0;
   auto window = [&](const Piece& pp, int base) -> int {
     const int jj = base + lane;
-    const long long off = S_rows ? S_rows[pp.i] : static_cast<long long>(pp.i) * P.max_blocks;
+    const long long off = kExt ? static_cast<long long>(S_rows[pp.i]) : static_cast<long long>(pp.i) * P.max_blocks;
     return jj < pp.j1 ? P.tables[off + jj] : 0;
   };
   auto prefetch_rows = [&](const Piece& pp) {
@@ -946,7 +947,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     }
     const long long row0 = (static_cast<long long>(pc.i) * P.Hq + pc.h * G) * kHeadDim;
     float* rec = P.ws + pc.rec * record_floats(G);
-    if (pc.final_out && P.lse && lane == 0) {
+    if (kExt && P.lse && pc.final_out && lane == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g)
         P.lse[static_cast<long long>(pc.i) * P.Hq + pc.h * G + g] = lg[g] > 0.f ? mg[g] + __log2f(lg[g]) : -INFINITY;
@@ -1304,7 +1305,7 @@ static void profile_release() {
   g_prof_next = 0;
 }
 
-template <int G, bool kBf16, bool kFused>
+template <int G, bool kBf16, bool kFused, bool kExt>
 static int occupancy_for(size_t bytes) {
   static std::mutex mu;
   static int cached_dev = -1;
@@ -1314,12 +1315,12 @@ static int occupancy_for(size_t bytes) {
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
   if (dev == cached_dev && bytes == cached_bytes) return cached_occ;
-  if (cudaFuncSetAttribute(decode_kernel<G, kBf16, kFused>,
+  if (cudaFuncSetAttribute(decode_kernel<G, kBf16, kFused, kExt>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes<G>(kMaxSplitSeqs, true))) != cudaSuccess)
     return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G, kBf16, kFused>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G, kBf16, kFused, kExt>,
                                                     Shape<G>::kThreads, bytes) != cudaSuccess)
     return 0;
   if (occ > kMaxCtasPerSm) occ = kMaxCtasPerSm;
@@ -1329,12 +1330,12 @@ static int occupancy_for(size_t bytes) {
   return occ;
 }
 
-template <int G, bool kBf16, bool kFused>
+template <int G, bool kBf16, bool kFused, bool kExt>
 static int launch_typed(Params& P, int device, cudaStream_t stream) {
   constexpr int NW = Shape<G>::NW;
   int B_smem = P.sched == SCHED_SEGMENT ? 0 : P.B;
   size_t bytes = smem_bytes<G>(B_smem, P.table_offs != nullptr);
-  int occ = occupancy_for<G, kBf16, kFused>(bytes);
+  int occ = occupancy_for<G, kBf16, kFused, kExt>(bytes);
   if (occ <= 0) return PA_ERR_CUDA;
   long long slots = static_cast<long long>(sm_count(device)) * occ;
   long long grid;
@@ -1354,7 +1355,7 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   P.lean_units = static_cast<int>(grid) * NW;
   const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
   if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
-  decode_kernel<G, kBf16, kFused><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
+  decode_kernel<G, kBf16, kFused, kExt><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   if (P.sched != SCHED_SEGMENT) {
     // the merge of split segments, as a programmatic dependent launch
@@ -1382,17 +1383,17 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-template <bool kBf16, bool kFused>
+template <bool kBf16, bool kFused, bool kExt>
 static int launch_g(int G, Params& P, int device, cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_typed<1, kBf16, kFused>(P, device, stream);
-    case 2: return launch_typed<2, kBf16, kFused>(P, device, stream);
-    case 3: return launch_typed<3, kBf16, kFused>(P, device, stream);
-    case 4: return launch_typed<4, kBf16, kFused>(P, device, stream);
-    case 5: return launch_typed<5, kBf16, kFused>(P, device, stream);
-    case 6: return launch_typed<6, kBf16, kFused>(P, device, stream);
-    case 7: return launch_typed<7, kBf16, kFused>(P, device, stream);
-    case 8: return launch_typed<8, kBf16, kFused>(P, device, stream);
+    case 1: return launch_typed<1, kBf16, kFused, kExt>(P, device, stream);
+    case 2: return launch_typed<2, kBf16, kFused, kExt>(P, device, stream);
+    case 3: return launch_typed<3, kBf16, kFused, kExt>(P, device, stream);
+    case 4: return launch_typed<4, kBf16, kFused, kExt>(P, device, stream);
+    case 5: return launch_typed<5, kBf16, kFused, kExt>(P, device, stream);
+    case 6: return launch_typed<6, kBf16, kFused, kExt>(P, device, stream);
+    case 7: return launch_typed<7, kBf16, kFused, kExt>(P, device, stream);
+    case 8: return launch_typed<8, kBf16, kFused, kExt>(P, device, stream);
     default: return PA_ERR_UNSUPPORTED;
   }
 }
@@ -1469,9 +1470,18 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.wait_limit_ns = wait_limit_ns();
   cudaStream_t st = as_stream(stream);
   const bool bf16 = p->dtype == PA_BF16;
-  if (bf16)
-    return fused ? launch_g<true, true>(G, P, p->device, st) : launch_g<true, false>(G, P, p->device, st);
-  return fused ? launch_g<false, true>(G, P, p->device, st) : launch_g<false, false>(G, P, p->device, st);
+  {
+    // table offsets (and, optionally, log2-sum-exp outputs) select the
+    // extended kernel; the plain and fused kernels carry neither
+    const bool ext = table_offs != nullptr;
+    if (lse && !ext) return PA_ERR_INVALID;
+    if (bf16) {
+      if (ext) return launch_g<true, false, true>(G, P, p->device, st);
+      return fused ? launch_g<true, true, false>(G, P, p->device, st) : launch_g<true, false, false>(G, P, p->device, st);
+    }
+    if (ext) return launch_g<false, false, true>(G, P, p->device, st);
+    return fused ? launch_g<false, true, false>(G, P, p->device, st) : launch_g<false, false, false>(G, P, p->device, st);
+  }
 }
 
 }  // namespace pa
