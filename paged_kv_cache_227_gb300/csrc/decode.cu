@@ -573,9 +573,13 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   const int k_tok = lr + 8 * (lm & 1), k_cadd = lm >> 1;
   // ldmatrix.trans of V^T: matrix lm covers tokens 8*(lm/2).. and dims 8*(lm%2).. of an m-tile
   const int v_tok = lr + 8 * (lm >> 1), v_cadd = lm & 1;
-  // value product on the tensor cores when the high and low weight halves of
-  // all heads fit the 8 columns of one m16n8k16 product
-  constexpr bool kMmaPv = G <= 4;
+  // Value product.  Mode 1 (G <= 4): tensor cores, the high and low weight
+  // halves of all heads in the 8 columns of one m16n8k16 product.  Mode 2
+  // (G > 4, extended kernel): tensor cores, the high halves and the low
+  // halves in one product each.  Mode 0 (G > 4): packed fp32 FMAs, measured
+  // faster than mode 2 for the plain decode of G = 6.
+  constexpr int kPvMode = G <= 4 ? 1 : (kExt ? 2 : 0);
+  constexpr bool kMmaPv = kPvMode != 0;
   // value phase: lane owns 16-byte chunk c16 of the V rows of token parity r16
   const int c16 = lane & 15;
   const int r16 = lane >> 4;
@@ -700,10 +704,15 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     // high halves and columns 4-7 the low halves of the weights of heads 0-3.
     // FMA path (G > 4): o[g][e] holds dims 8*c16+2e, +1 of head g over the
     // tokens of parity r16.
+    // Mode 2: oc holds the products with the high halves of all 8 columns
+    // (heads 2c4, 2c4+1 for this lane), oc2 those with the low halves.
     float oc[kMmaPv ? 8 : 1][4];
+    float oc2[kPvMode == 2 ? 8 : 1][4];
     float2 o[kMmaPv ? 1 : G][4];
 #pragma unroll
     for (int mt = 0; mt < (kMmaPv ? 8 : 1); ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < (kPvMode == 2 ? 8 : 1); ++mt) oc2[mt][0] = oc2[mt][1] = oc2[mt][2] = oc2[mt][3] = 0.f;
 #pragma unroll
     for (int g = 0; g < (kMmaPv ? 1 : G); ++g)
 #pragma unroll
@@ -798,7 +807,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
             l_run[c] *= alpha[c];
             m_run[c] = mn;
           }
-          if constexpr (kMmaPv) {
+          if constexpr (kPvMode == 1) {
             // columns 4-7 (low halves) belong to the heads of lane c4 - 2
             const float x0 = __shfl_xor_sync(0xffffffffu, alpha[0], 2);
             const float x1 = __shfl_xor_sync(0xffffffffu, alpha[1], 2);
@@ -809,6 +818,18 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
               oc[mt][1] *= a1;
               oc[mt][2] *= a0;
               oc[mt][3] *= a1;
+            }
+          } else if constexpr (kPvMode == 2) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              oc[mt][0] *= alpha[0];
+              oc[mt][1] *= alpha[1];
+              oc[mt][2] *= alpha[0];
+              oc[mt][3] *= alpha[1];
+              oc2[mt][0] *= alpha[0];
+              oc2[mt][1] *= alpha[1];
+              oc2[mt][2] *= alpha[0];
+              oc2[mt][3] *= alpha[1];
             }
           } else {
 #pragma unroll
@@ -850,7 +871,22 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
           scores((n + 1) % SW, acc2);
       }
       if (cur_blk >= 0) {
-        if constexpr (kMmaPv) {
+        if constexpr (kPvMode == 2) {
+          // ---- O^T += V^T P on the tensor cores, 8 heads: the high 16-bit
+          // halves of the weights in one product, the low halves in another
+          const uint32_t bh0 = movmatrix_trans(pack_hi<kBf16>(p[0], p[1]));
+          const uint32_t bh1 = movmatrix_trans(pack_hi<kBf16>(p[2], p[3]));
+          const uint32_t bl0 = movmatrix_trans(pack_lo<kBf16>(p[0], p[1]));
+          const uint32_t bl1 = movmatrix_trans(pack_lo<kBf16>(p[2], p[3]));
+          const uint32_t vs_addr = smem_addr(Vs);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(vs_addr + swz(v_tok, 2 * mt + v_cadd), a0, a1, a2, a3);
+            mma16816<kBf16>(oc[mt], a0, a1, a2, a3, bh0, bh1);
+            mma16816<kBf16>(oc2[mt], a0, a1, a2, a3, bl0, bl1);
+          }
+        } else if constexpr (kPvMode == 1) {
           // ---- O^T += V^T P on the tensor cores.  B operand: the weights as
           // a 16-token x 8-column matrix (columns 0-3: high 16-bit halves of
           // heads 0-3, columns 4-7: the low halves, so hi + lo carries p to
@@ -952,7 +988,33 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       for (int g = 0; g < G; ++g)
         P.lse[static_cast<long long>(pc.i) * P.Hq + pc.h * G + g] = lg[g] > 0.f ? mg[g] + __log2f(lg[g]) : -INFINITY;
     }
-    if constexpr (kMmaPv) {
+    if constexpr (kPvMode == 2) {
+      // o = high + low products; lane c4 holds heads 2c4, 2c4+1 at dims
+      // 16mt+r4 (entries 0, 1) and 16mt+r4+8 (entries 2, 3)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int g = 2 * c4 + e;
+        if (g < G) {
+          float lgg = lg[0];
+#pragma unroll
+          for (int gg = 1; gg < G; ++gg)
+            if (g == gg) lgg = lg[gg];
+          const float inv = lgg > 0.f ? 1.f / lgg : 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float v = oc[mt][2 * hh + e] + oc2[mt][2 * hh + e];
+              const int d = 16 * mt + r4 + 8 * hh;
+              if (pc.final_out)
+                store_out(P.out, row0 + g * kHeadDim + d, v * inv, P.out_dtype);
+              else
+                rec[g * kHeadDim + d] = v;
+            }
+          }
+        }
+      }
+    } else if constexpr (kPvMode == 1) {
       // o = high + low columns; lanes c4 and c4^2 then hold the same sums:
       // lane c4 < 2 writes dims 16mt+r4, lane c4 >= 2 dims 16mt+r4+8, of
       // heads 2(c4&1) and 2(c4&1)+1
