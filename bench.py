@@ -444,7 +444,8 @@ def run_multi_query(args):
     q = torch.randn(n_q, cfg.n_q_heads, cfg.d_head, generator=g).to(cfg.torch_dtype).to(device)
     out = torch.empty_like(q)
     qs, bt, sl = (torch.from_numpy(x).to(device) for x in (q_start, tables, dec_lens))
-    ws = torch.empty(pa.lib.pa_decode_multi_workspace_bytes(pool.handle, n_q, cfg.n_q_heads, tables.shape[1]),
+    ws = torch.empty(pa.lib.pa_decode_multi_workspace_bytes(pool.handle, n_q, len(dec_lens), cfg.n_q_heads,
+                                                             tables.shape[1]),
                      dtype=torch.uint8, device=device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)

@@ -188,14 +188,16 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
  * Row r = q_start[i] + t sits at position L_i - T_i + t and attends over
  * positions 0 .. L_i - T_i + t (causal within the new tokens):
  *   out[r][h] = softmax(scale * K[0..p] q[r][h]) V[0..p],  p = L_i - T_i + t.
- * out: device [n_q][n_q_heads][128] in out_dtype.  Each row is one unit of
- * the balanced split (so the rows of a sequence read their common prefix
- * close together in time; repeated reads are served from L2).  workspace:
+ * out: device [n_q][n_q_heads][128] in out_dtype.  A sequence's new tokens
+ * are packed 8/G at a time into the columns of one segment of the balanced
+ * split (G = n_q_heads / n_kv_heads), each column masked to its token's causal
+ * prefix, so every K/V tile is read once per 8/G new tokens.  workspace:
  * device, >= pa_decode_multi_workspace_bytes(...) bytes, 256-byte aligned.
- * n_q <= 4096 (else PA_ERR_UNSUPPORTED).  A row with T_i > L_i, or a length
- * out of range, records PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros. */
-size_t pa_decode_multi_workspace_bytes(pa_pool_t pool, int n_q, int n_q_heads,
-                                       int max_blocks_per_seq);
+ * ceil(n_q / (8/G)) + num_seqs <= 4096 (else PA_ERR_UNSUPPORTED).  A
+ * sequence with T_i > L_i, or a length out of range, records
+ * PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros. */
+size_t pa_decode_multi_workspace_bytes(pa_pool_t pool, int n_q, int num_seqs,
+                                       int n_q_heads, int max_blocks_per_seq);
 int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n_q,
                     const int32_t* block_tables, int max_blocks_per_seq,
                     const int32_t* seq_lens, int num_seqs, int n_q_heads,

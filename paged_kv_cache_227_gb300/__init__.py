@@ -51,7 +51,7 @@ def _load():
         "pa_decode_workspace_bytes": (sz, [vp, i32, i32, i32, i32]),
         "pa_decode_split": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
         "pa_append_decode": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp, sz, vp]),
-        "pa_decode_multi_workspace_bytes": (ctypes.c_size_t, [vp, i32, i32, i32]),
+        "pa_decode_multi_workspace_bytes": (ctypes.c_size_t, [vp, i32, i32, i32, i32]),
         "pa_decode_multi": (i32, [vp, vp, vp, i32, vp, i32, vp, i32, i32, f32, vp, i32, vp, ctypes.c_size_t, vp]),
         "pa_decode_cascade_workspace_bytes": (ctypes.c_size_t, [vp, i32, i32, i32, i32]),
         "pa_decode_cascade": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, vp, vp, i32, vp, i32, vp,
@@ -262,7 +262,7 @@ def pa_decode_multi(pool, q, q_start, block_tables, seq_lens, scale, out, worksp
         raise ValueError("out must be [n_q][Hq][128] of fp16, bf16 or fp32")
     W = block_tables.shape[1]
     if workspace is None:
-        n = lib.pa_decode_multi_workspace_bytes(pool.handle, n_q, Hq, W)
+        n = lib.pa_decode_multi_workspace_bytes(pool.handle, n_q, B, Hq, W)
         if n == 0:
             raise PagedAttentionError(PA_ERR_INVALID, "pa_decode_multi_workspace_bytes")
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)

@@ -84,6 +84,8 @@ struct Params {
   const int32_t* tables;    // [rows][max_blocks]
   const int32_t* table_offs;  // [B]: element offset of sequence i's table row, or null (i * max_blocks)
   float* lse;               // [B][Hq] log2-sum-exp of the scaled scores (log2 units), or null
+  const int32_t* ext_ntok;  // [B]: query tokens packed in sequence i's columns, or null (1)
+  int ext_g;                // columns per packed token (the real group size)
   const int32_t* seq_lens;  // [B]
   void* out;                // [B][Hq][128]
   float* ws;                // partial records
@@ -457,7 +459,10 @@ __device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report, 
       L = L < 0 ? 0 : cap;
     }
     if (lens) lens[i] = L;
-    if (rows) rows[i] = P.table_offs[i];
+    if (rows) {
+      rows[i] = P.table_offs[i];
+      rows[P.B + i] = P.ext_ntok ? P.ext_ntok[i] : 1;
+    }
     const int nb = (L + kBlock - 1) / kBlock;
     pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
   }
@@ -512,7 +517,7 @@ static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() 
 // to align the base to 1024 bytes.
 template <int G>
 constexpr size_t smem_bytes(int B, bool rows = false) {
-  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>((rows ? 3 : 2) * B + 1) + 1024;
+  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>((rows ? 4 : 2) * B + 1) + 1024;
 }
 
 // ---------------------------------------------------------------------------
@@ -719,6 +724,18 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     const int nb_total = (pc.L + kBlock - 1) / kBlock;
+    // extended kernel: the sequence packs ntok query tokens, G / ntok columns
+    // each; token t of them sees ntok - 1 - t fewer positions (causal)
+    int cut0 = 0, cut1 = 0;
+    if constexpr (kExt) {
+      const int nt = S_rows[P.B + pc.i];
+      if (nt > 1) {
+        cut0 = nt - 1 - g0 / P.ext_g;
+        cut1 = nt - 1 - (g0 + 1) / P.ext_g;
+        cut0 = cut0 < 0 ? 0 : cut0;
+        cut1 = cut1 < 0 ? 0 : cut1;
+      }
+    }
 
     // prepare(): wait for the tile's stage, read its block id, put the new
     // token into the tile and the pool (fused append), and on the tensor-core
@@ -791,8 +808,11 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
         float mx[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          st[c] = r4 < valid_tokens ? st[c] * P.qscale : -INFINITY;
-          st[2 + c] = r4 + 8 < valid_tokens ? st[2 + c] * P.qscale : -INFINITY;
+          // (rows past a column's last position; the cut can reach into the
+          // tile before the last one)
+          const int vt = kExt ? pc.L - j * kBlock - (c ? cut1 : cut0) : valid_tokens;
+          st[c] = r4 < vt ? st[c] * P.qscale : -INFINITY;
+          st[2 + c] = r4 + 8 < vt ? st[2 + c] * P.qscale : -INFINITY;
           mx[c] = fmaxf(st[c], st[2 + c]);
 #pragma unroll
           for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
@@ -803,7 +823,9 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const float mn = fmaxf(m_run[c], mx[c]);
-            alpha[c] = fast_exp2(m_run[c] - mn);
+            // (extended kernel: a column with no position seen yet stays at
+            // -inf and keeps its zero state)
+            alpha[c] = kExt && mn == -INFINITY ? 1.f : fast_exp2(m_run[c] - mn);
             l_run[c] *= alpha[c];
             m_run[c] = mn;
           }
@@ -845,7 +867,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          p[k] = fast_exp2(st[k] - m_run[k & 1]);
+          // (extended kernel: a column may see no position of a piece yet)
+          p[k] = kExt && st[k] == -INFINITY ? 0.f : fast_exp2(st[k] - m_run[k & 1]);
           l_run[k & 1] += p[k];
         }
         if constexpr (!kMmaPv) {
@@ -1191,31 +1214,123 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Several new query tokens per sequence: each query row becomes its own
-// (virtual) sequence that reads its owner's table row over the causal prefix
-// it may see.  Row r of sequence i (q_start[i] <= r < q_start[i+1], T_i rows)
-// sits at position L_i - T_i + (r - q_start[i]) and attends over that many
-// tokens plus one.
+// Several new query tokens per sequence.  Sequence i's T_i new tokens are its
+// last T_i positions; token t sees positions 0 .. L_i - T_i + t.  They are
+// packed TC at a time (TC = 8 / G) into the columns of one extended-kernel
+// segment: packed sequence v holds tokens t0 .. t0 + ntok - 1 of sequence i,
+// its length is the last token's position + 1, column tt*G + g is token
+// t0 + tt's query head g, and token t0 + tt sees ntok - 1 - tt positions
+// fewer.  Every K/V tile of the prefix is read once per TC tokens.
 // ---------------------------------------------------------------------------
-__global__ void multi_prep_kernel(const int32_t* __restrict__ q_start, const int32_t* __restrict__ seq_lens,
-                                  int B, int n_q, int cap, int32_t* __restrict__ lens_out,
-                                  int32_t* __restrict__ rows_out, long long* err) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= n_q) return;
-  int lo = 0, hi = B - 1;  // the last i with q_start[i] <= r
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (q_start[mid] <= r) lo = mid; else hi = mid - 1;
+struct MultiPlan {
+  const int32_t* q_start;   // [B + 1]
+  const int32_t* seq_lens;  // [B]
+  int B, n_q, TC, Bv, max_blocks;
+  int32_t* lens_v;          // [Bv]
+  int32_t* offs_v;          // [Bv]
+  int32_t* ntok_v;          // [Bv]
+  int32_t* qrow;            // [Bv * TC]: query row of column block tt, or -1
+  int32_t* rowmap;          // [n_q]: v * TC + tt of query row r
+  long long* err;
+};
+
+// One CTA: packed sequences in sequence order (a block-wide scan of
+// ceil(T_i / TC)), then the unused tail of the Bv slots.
+__global__ void __launch_bounds__(1024) multi_plan_kernel(MultiPlan M) {
+  __shared__ int warp_sum[32];
+  __shared__ int carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int cap = M.max_blocks * kBlock;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < M.B; base += blockDim.x) {
+    const int i = base + tid;
+    int T = 0, L = 0, V = 0;
+    if (i < M.B) {
+      T = M.q_start[i + 1] - M.q_start[i];
+      L = M.seq_lens[i];
+      V = T > 0 ? (T + M.TC - 1) / M.TC : 0;
+    }
+    int incl = V;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int w = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int start = carry_s + (wid ? warp_sum[wid - 1] : 0) + incl - V;
+    if (i < M.B && V > 0) {
+      const bool bad = L < T || L > cap || start + V > M.Bv;
+      if (bad) record_error(M.err, PA_ERR_DEVICE_CHECK, i);
+      for (int k = 0; k < V && start + k < M.Bv; ++k) {
+        const int v = start + k, t0 = k * M.TC;
+        const int nt = T - t0 < M.TC ? T - t0 : M.TC;
+        M.lens_v[v] = bad ? 0 : L - T + t0 + nt;
+        M.offs_v[v] = i * M.max_blocks;
+        M.ntok_v[v] = nt;
+        for (int tt = 0; tt < M.TC; ++tt) {
+          const int r = M.q_start[i] + t0 + tt;
+          const bool real = tt < nt && r >= 0 && r < M.n_q;
+          M.qrow[v * M.TC + tt] = real ? r : -1;
+          if (real) M.rowmap[r] = v * M.TC + tt;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0) carry_s += warp_sum[(blockDim.x >> 5) - 1];
+    __syncthreads();
   }
-  const int T = q_start[lo + 1] - q_start[lo];
-  int L = seq_lens[lo];
-  int len = L - T + (r - q_start[lo]) + 1;
-  if (L < 0 || L > cap || T <= 0 || len < 1 || len > L) {
-    record_error(err, PA_ERR_DEVICE_CHECK, static_cast<long long>(r));
-    len = 0;  // an all-zero output row
+  for (int v = carry_s + tid; v < M.Bv; v += blockDim.x) {
+    M.lens_v[v] = 0;
+    M.offs_v[v] = 0;
+    M.ntok_v[v] = 1;
+    for (int tt = 0; tt < M.TC; ++tt) M.qrow[v * M.TC + tt] = -1;
   }
-  lens_out[r] = len;
-  rows_out[r] = lo * (cap / kBlock);  // element offset of the owner's table row
+}
+
+// q of the packed sequences: row (v*Hkv + h)*GP + tt*G + g, zero for unused
+// column blocks.  One thread per 16-byte vector.
+__global__ void multi_pack_kernel(const uint4* __restrict__ q, const int32_t* __restrict__ qrow, int Bv, int Hkv,
+                                  int G, int TC, int Hq, uint4* __restrict__ qv) {
+  const int GP = G * TC;
+  const long long n_vec = static_cast<long long>(Bv) * Hkv * GP * (kHeadDim / 8);
+  for (long long x = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; x < n_vec;
+       x += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = x / (kHeadDim / 8);
+    const int w = static_cast<int>(x % (kHeadDim / 8));
+    const int col = static_cast<int>(row % GP);
+    const long long vh = row / GP;
+    const int h = static_cast<int>(vh % Hkv);
+    const long long v = vh / Hkv;
+    const int r = qrow[v * TC + col / G];
+    qv[x] = r >= 0 ? q[((static_cast<long long>(r) * Hq + h * G + col % G) * kHeadDim) / 8 + w]
+                   : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// One warp per (query row, query head): out[r][hq] from the packed output.
+__global__ void multi_unpack_kernel(const float* __restrict__ ov, const int32_t* __restrict__ rowmap, int n_q,
+                                    int Hkv, int G, int TC, void* out, int out_dtype) {
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Hq = Hkv * G, GP = G * TC;
+  if (wid >= static_cast<long long>(n_q) * Hq) return;
+  const int r = static_cast<int>(wid / Hq), hq = static_cast<int>(wid % Hq);
+  const int vt = rowmap[r];
+  const long long src = (static_cast<long long>(vt / TC) * Hkv + hq / G) * GP + (vt % TC) * G + hq % G;
+  const float4 o = reinterpret_cast<const float4*>(ov + src * kHeadDim)[lane];
+  store_out4(out, wid * kHeadDim + 4 * lane, o.x, o.y, o.z, o.w, out_dtype);
 }
 
 // ---------------------------------------------------------------------------
@@ -1487,7 +1602,8 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
                          const int32_t* tables, int max_blocks, const int32_t* seq_lens, int B,
                          int Hq, float scale, void* out, int out_dtype, int sched,
                          int partition_blocks, void* ws, size_t ws_bytes, void* stream,
-                         const int32_t* table_offs = nullptr, float* lse = nullptr) {
+                         const int32_t* table_offs = nullptr, float* lse = nullptr,
+                         const int32_t* ext_ntok = nullptr, int ext_g = 0) {
   if (!p || !q || !tables || !seq_lens || !out || B <= 0 || Hq <= 0 || max_blocks <= 0)
     return PA_ERR_INVALID;
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
@@ -1515,6 +1631,8 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.tables = tables;
   P.table_offs = table_offs;
   P.lse = lse;
+  P.ext_ntok = ext_ntok;
+  P.ext_g = ext_g > 0 ? ext_g : 1;
   P.seq_lens = seq_lens;
   P.out = out;
   P.ws = static_cast<float*>(ws);
@@ -1616,39 +1734,92 @@ int pa_append_decode(pa_pool_t p, const void* q, const void* k_new, const void* 
                        workspace_bytes, stream);
 }
 
-// Multi-token queries: workspace = per-row lengths and table rows (int32
-// each, 256-byte aligned), then the balanced split's partial records.
-static size_t multi_head_bytes(int n_q) {
-  return (sizeof(int32_t) * 2 * static_cast<size_t>(n_q) + 255) / 256 * 256;
+// Multi-token queries: workspace pieces, each 256-byte aligned.
+struct MultiLayout {
+  int TC, Bv;
+  size_t lens_v, offs_v, ntok_v, qrow, rowmap, qv, ov, rec, total;
+};
+static bool multi_layout(const pa_pool* p, int n_q, int B, int Hq, int max_blocks, MultiLayout* L) {
+  if (!p || n_q <= 0 || B <= 0 || Hq <= 0 || max_blocks <= 0 || Hq % p->n_kv_heads) return false;
+  const int G = Hq / p->n_kv_heads;
+  if (G > PA_MAX_GROUP) return false;
+  L->TC = PA_MAX_GROUP / G;
+  L->Bv = (n_q + L->TC - 1) / L->TC + B;  // every sequence's last pack may be partial
+  const int GP = G * L->TC;
+  WorkspaceLayout rw{};
+  if (!workspace_layout(p, L->Bv, p->n_kv_heads * GP, max_blocks, 0, &rw)) return false;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  const size_t rows_v = static_cast<size_t>(L->Bv) * p->n_kv_heads * GP;
+  L->lens_v = take(sizeof(int32_t) * L->Bv);
+  L->offs_v = take(sizeof(int32_t) * L->Bv);
+  L->ntok_v = take(sizeof(int32_t) * L->Bv);
+  L->qrow = take(sizeof(int32_t) * static_cast<size_t>(L->Bv) * L->TC);
+  L->rowmap = take(sizeof(int32_t) * static_cast<size_t>(n_q));
+  L->qv = take(rows_v * kHeadDim * 2);
+  L->ov = take(rows_v * kHeadDim * 4);
+  L->rec = take(rw.total);
+  L->total = off;
+  return true;
 }
 
-size_t pa_decode_multi_workspace_bytes(pa_pool_t p, int n_q, int n_q_heads, int max_blocks_per_seq) {
-  WorkspaceLayout lay{};
-  if (!p || n_q <= 0 || !workspace_layout(p, n_q, n_q_heads, max_blocks_per_seq, 0, &lay)) return 0;
-  return multi_head_bytes(n_q) + lay.total;
+size_t pa_decode_multi_workspace_bytes(pa_pool_t p, int n_q, int num_seqs, int n_q_heads, int max_blocks_per_seq) {
+  MultiLayout L{};
+  return multi_layout(p, n_q, num_seqs, n_q_heads, max_blocks_per_seq, &L) ? L.total : 0;
 }
 
 int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
                     int num_seqs, int n_q_heads, float scale, void* out, int out_dtype,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  if (!p || !q_start || !seq_lens || !block_tables || num_seqs <= 0 || n_q <= 0 || max_blocks_per_seq <= 0)
+  if (!p || !q || !out || !q_start || !seq_lens || !block_tables || num_seqs <= 0 || n_q <= 0 ||
+      max_blocks_per_seq <= 0)
     return PA_ERR_INVALID;
-  if (n_q > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
-  const size_t need = pa_decode_multi_workspace_bytes(p, n_q, n_q_heads, max_blocks_per_seq);
-  if (need == 0) return PA_ERR_INVALID;
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+  if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PA_ERR_INVALID;
+  MultiLayout L{};
+  if (!multi_layout(p, n_q, num_seqs, n_q_heads, max_blocks_per_seq, &L)) return PA_ERR_INVALID;
+  if (num_seqs > kMaxSplitSeqs || L.Bv > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return PA_ERR_INVALID;
-  int32_t* lens = static_cast<int32_t*>(workspace);
-  int32_t* rows = lens + n_q;
+  char* ws = static_cast<char*>(workspace);
+  const int Hkv = p->n_kv_heads, G = n_q_heads / Hkv, GP = G * L.TC;
+  MultiPlan M{};
+  M.q_start = q_start;
+  M.seq_lens = seq_lens;
+  M.B = num_seqs;
+  M.n_q = n_q;
+  M.TC = L.TC;
+  M.Bv = L.Bv;
+  M.max_blocks = max_blocks_per_seq;
+  M.lens_v = reinterpret_cast<int32_t*>(ws + L.lens_v);
+  M.offs_v = reinterpret_cast<int32_t*>(ws + L.offs_v);
+  M.ntok_v = reinterpret_cast<int32_t*>(ws + L.ntok_v);
+  M.qrow = reinterpret_cast<int32_t*>(ws + L.qrow);
+  M.rowmap = reinterpret_cast<int32_t*>(ws + L.rowmap);
+  M.err = p->err;
   cudaStream_t st = as_stream(stream);
-  multi_prep_kernel<<<(n_q + 255) / 256, 256, 0, st>>>(q_start, seq_lens, num_seqs, n_q, max_blocks_per_seq * kBlock,
-                                                       lens, rows, p->err);
+  // rows the plan never maps (a broken q_start) read packed row 0 of sequence 0
+  if (cudaMemsetAsync(M.rowmap, 0, sizeof(int32_t) * static_cast<size_t>(n_q), st) != cudaSuccess) return PA_ERR_CUDA;
+  multi_plan_kernel<<<1, 1024, 0, st>>>(M);
+  const long long n_vec = static_cast<long long>(L.Bv) * Hkv * GP * (kHeadDim / 8);
+  const int pack_grid = static_cast<int>(n_vec < 4096 * 256 ? (n_vec + 255) / 256 : 4096);
+  multi_pack_kernel<<<pack_grid, 256, 0, st>>>(static_cast<const uint4*>(q), M.qrow, L.Bv, Hkv, G, L.TC, n_q_heads,
+                                               reinterpret_cast<uint4*>(ws + L.qv));
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  const size_t head = multi_head_bytes(n_q);
-  return decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, lens, n_q, n_q_heads, scale, out,
-                       out_dtype, SCHED_LEAN, 0, static_cast<char*>(workspace) + head, workspace_bytes - head,
-                       stream, rows);
+  float* ov = reinterpret_cast<float*>(ws + L.ov);
+  const int rc = decode_common(p, ws + L.qv, nullptr, nullptr, block_tables, max_blocks_per_seq, M.lens_v, L.Bv,
+                               Hkv * GP, scale, ov, PA_FP32, SCHED_LEAN, 0, ws + L.rec, L.total - L.rec, stream,
+                               M.offs_v, nullptr, M.ntok_v, G);
+  if (rc != PA_OK) return rc;
+  const long long warps = static_cast<long long>(n_q) * n_q_heads;
+  multi_unpack_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(ov, M.rowmap, n_q, Hkv, G, L.TC,
+                                                                                     out, out_dtype);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 // Shared-prefix decode: workspace pieces, each 256-byte aligned.
