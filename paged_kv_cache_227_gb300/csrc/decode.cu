@@ -602,6 +602,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   int ij = ihave ? ip.j0 : 0;
   int tb_base = ij, tb_val = 0, tb_nv = 0;
   int n_issued = 0;
+  bool append_seen = false;  // fused step: the append grid has completed
   auto window = [&](const Piece& pp, int base) -> int {
     const int jj = base + lane;
     const long long off = kExt ? static_cast<long long>(S_rows[pp.i]) : static_cast<long long>(pp.i) * P.max_blocks;
@@ -609,13 +610,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   };
   auto prefetch_rows = [&](const Piece& pp) {
     const long long qrow = (static_cast<long long>(pp.i) * P.Hq + pp.h * G) * kHeadDim;
-    if (lane < 2 * G) {
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + qrow + 64 * lane));
-    } else if (kFused && lane < 2 * G + 4) {
-      const int r = lane - 2 * G;
-      const long long nrow = (static_cast<long long>(pp.i) * P.Hkv + pp.h) * kHeadDim + 64 * (r & 1);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"((r < 2 ? P.k_new : P.v_new) + nrow));
-    }
+    if (lane < 2 * G) asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + qrow + 64 * lane));
   };
   auto load_following = [&]() {
     if (tb_base + 32 < ip.j1) {
@@ -647,6 +642,12 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       load_following();
     }
     const int blk = __shfl_sync(0xffffffffu, tb_val, ij - tb_base);
+    if (kFused && !append_seen && ij == (ip.L + kBlock - 1) / kBlock - 1) {
+      // the sequence's last tile holds its new token, which the append grid
+      // (this grid's programmatic prerequisite) writes: wait for it once
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      append_seen = true;
+    }
     if (lane == 0) {
       const bool valid = blk >= 0 && blk < P.num_blocks;
       S.stage_blk[warp][stage] = valid ? blk : -1;
@@ -683,19 +684,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
     }
   };
-  // fused append: this lane's 16 bytes of the new K (lanes 0-15) or V row,
-  // fetched when the piece that holds the sequence's last tile starts
-  uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
-  auto load_new = [&]() {
-    if (kFused && pc.L > 0 && pc.j1 == (pc.L + kBlock - 1) / kBlock) {
-      const long long src = (static_cast<long long>(pc.i) * P.Hkv + pc.h) * kHeadDim;
-      newrow = *reinterpret_cast<const uint4*>((lane < 16 ? P.k_new : P.v_new) + src + 8 * c16);
-    }
-  };
-  if (have_pc) {  // in flight while the first loads are issued
-    load_q();
-    load_new();
-  }
+  if (have_pc) load_q();  // in flight while the first loads are issued
 #pragma unroll 1
   for (int s = 0; s < SW; ++s) issue(s);
 
@@ -737,10 +726,9 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       }
     }
 
-    // prepare(): wait for the tile's stage, read its block id, put the new
-    // token into the tile and the pool (fused append), and on the tensor-core
-    // path clear the V rows past the sequence's end (0 x NaN would poison
-    // the product; the weights there are exactly zero).
+    // prepare(): wait for the tile's stage, read its block id, and on the
+    // tensor-core path clear the V rows past the sequence's end (0 x NaN would
+    // poison the product; the weights there are exactly zero).
     auto prepare = [&](int jj, int nn, int& blk_out, bool& touched_out) -> bool {
       const int s = nn % SW;
       const uint32_t parity = static_cast<uint32_t>((nn / SW) & 1);
@@ -753,16 +741,6 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       blk_out = blk;
       if (blk >= 0 && jj == nb_total - 1) {
         uint8_t* Ks = ring + s * kStageBytes;
-        if (kFused) {
-          // the new token: the caller's k_new/v_new for position L-1, also
-          // written to its slot in the pool
-          const int tn = (pc.L - 1) & (kBlock - 1);
-          const long long dst = ((static_cast<long long>(blk) * P.Hkv + pc.h) * kBlock + tn) * kHeadDim;
-          *reinterpret_cast<uint4*>((lane < 16 ? Ks : Ks + kTileBytes) + swz(tn, c16)) = newrow;
-          uint16_t* pool_w = const_cast<uint16_t*>(lane < 16 ? P.k_pool : P.v_pool);
-          *reinterpret_cast<uint4*>(pool_w + dst + 8 * c16) = newrow;
-          touched_out = true;
-        }
         const int valid = pc.L - jj * kBlock;
         if (kMmaPv && valid < kBlock) {
           for (int x = valid * 16 + lane; x < kBlock * 16; x += 32)
@@ -1110,11 +1088,11 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       }
     }
     have_pc = cit.next(pc);
-    if (have_pc) {
-      load_q();
-      load_new();
-    }
+    if (have_pc) load_q();
   }
+
+  // fused step: this grid completes only after the append grid
+  if (kFused && blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // --- drain: never leave a bulk copy in flight into this warp's ring -------
   if (!ok && lane == 0) {
@@ -1532,7 +1510,27 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   P.lean_units = static_cast<int>(grid) * NW;
   const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
   if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
-  decode_kernel<G, kBf16, kFused, kExt><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
+  if (kFused) {
+    // the cache write first; the decode is its programmatic dependent and
+    // waits for it only before a tile that holds a new token
+    const int rc = launch_append_tail(const_cast<uint16_t*>(P.k_pool), const_cast<uint16_t*>(P.v_pool), P.Hkv,
+                                      P.num_blocks, P.err, device, P.k_new, P.v_new, P.tables, P.max_blocks,
+                                      P.seq_lens, P.B, stream);
+    if (rc != PA_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Shape<G>::kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel<G, kBf16, kFused, kExt>, P) != cudaSuccess) return PA_ERR_CUDA;
+  } else {
+    decode_kernel<G, kBf16, kFused, kExt><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
+  }
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   if (P.sched != SCHED_SEGMENT) {
     // the merge of split segments, as a programmatic dependent launch

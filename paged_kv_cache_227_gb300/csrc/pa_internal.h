@@ -53,4 +53,11 @@ int sm_count(int device);
 // Wait limit for bounded in-kernel waits, in nanoseconds.
 long long wait_limit_ns();
 
+// The fused step's cache write (one new token per sequence at position
+// L_i - 1), launched on `stream`; the decode follows as its programmatic
+// dependent.
+int launch_append_tail(void* k_pool, void* v_pool, int n_kv_heads, long long num_blocks, long long* err,
+                       int device, const void* k_new, const void* v_new, const int32_t* tables,
+                       int max_blocks, const int32_t* seq_lens, int B, cudaStream_t stream);
+
 }  // namespace pa
