@@ -212,7 +212,7 @@ def run_ours(args, rank, world, local):
             ctypes.c_void_p(sl.data_ptr()), q.shape[0], q.shape[1], float(case.scale),
             ctypes.c_void_p(out.data_ptr()), pa._DTYPE_CODE[out.dtype], args.partition_blocks,
             ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
-    launches_per_step = 2  # the decode kernel and the merge of split segments
+    launches_per_step = 3  # the append, the decode (its dependent) and the merge of split segments
 
     def step():
         code = fn(*argv)
@@ -384,14 +384,14 @@ def main():
             if cfg.key == 3 else str(cfg.lengths),
             "tokens_attended": int(np.sum(r["dec_lens"])),
             "pool_blocks": r["case"].num_blocks,
-            "step": "pa_append_decode (fused append + balanced split-KV decode + LSE merge)",
+            "step": "pa_append_decode (append, then balanced split-KV decode and LSE merge as dependent launches)",
             "partition_blocks": args.partition_blocks,
             "l2": f"flushed before every timed step (read of a {2 * r['l2'] >> 20} MiB buffer)",
             "bytes_per_step": nb,
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_kernel (fused append + split decode) + merge_kernel, one step",
+            "kernel": "append_tail_kernel + decode_kernel + merge_kernel (dependent launches), one step",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"

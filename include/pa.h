@@ -165,11 +165,12 @@ int pa_decode_split(pa_pool_t pool, const void* q, const int32_t* block_tables,
 
 /* Fused append + split decode for one new token per sequence.  seq_lens
  * counts the new token (L >= 1); the new token sits at position L-1, whose
- * slot is block_tables[i][(L-1)/16]*16 + (L-1)%16.  The kernel writes
- * k_new[i]/v_new[i] ([num_seqs][n_kv_heads][128]) to that slot and attends
- * over positions 0..L-1 using the input k_new/v_new for position L-1 (it never
- * reads back its own write).  The result equals pa_cache_append followed by
- * pa_decode_split.  Rows with L == 0 write nothing and output zeros. */
+ * slot is block_tables[i][(L-1)/16]*16 + (L-1)%16.  A small kernel writes
+ * k_new[i]/v_new[i] ([num_seqs][n_kv_heads][128]) to that slot; the decode is
+ * launched as its programmatic dependent, streams every other tile at once
+ * and waits for the write only before a tile that holds a new token.  The
+ * result equals pa_cache_append followed by pa_decode_split.  Rows with
+ * L == 0 write nothing and output zeros. */
 int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
                      const void* v_new, const int32_t* block_tables,
                      int max_blocks_per_seq, const int32_t* seq_lens,
