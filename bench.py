@@ -279,6 +279,7 @@ def run_ours(args, rank, world, local):
     return dict(cfg=cfg, case=case, dec_lens=dec_lens, tables=tables, nbytes=nbytes, total_bytes=total_bytes,
                 mean_ms=mean_ms,
                 p10=float(np.percentile(step_ms, 10)), p90=float(np.percentile(step_ms, 90)),
+                median=float(np.median(step_ms)),
                 kern_ms=kern_mean, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, wall=wall, clocks=clock_info,
                 launches=launches_per_step * K, K=K, l2=l2)
 
@@ -370,6 +371,7 @@ def main():
         "ms_per_step": round(r["mean_ms"], 5),
         "us_per_step": round(r["mean_ms"] * 1e3, 2),
         "us_per_step_p10_p90": [round(r["p10"] * 1e3, 2), round(r["p90"] * 1e3, 2)],
+        "us_per_step_median": round(r["median"] * 1e3, 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -419,6 +421,12 @@ def main():
         line["cpu_baseline"] = {"value": round(smp.bytes_of(n) * reps / dt / 1e9, 4), "unit": "GB/s",
                                 "cores": threads, "kind": "oracle",
                                 "sample": smp.describe(n, reps) + f", {dt:.1f} s"}
+        # the same oracle on one thread, on a sample sized for about 3 s
+        one = OracleSample(cfg, r["case"], r["tables"], r["dec_lens"], 1)
+        n1, reps1 = one.size_for(3.0)
+        dt1 = one.run(n1, reps1)
+        line["cpu_baseline"]["one_thread"] = {"value": round(one.bytes_of(n1) * reps1 / dt1 / 1e9, 4),
+                                              "sample": one.describe(n1, reps1) + f", {dt1:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -504,14 +512,16 @@ def run_cascade(args):
              "split": lambda: pa.pa_decode_split(pool, q, bt, sl, case.scale, out, 0, ws_s)}
     K = max(1, min(args.steps, 500))
     res = {}
-    for name, fn in calls.items():
+    for name, fn, flush in [(n, f, True) for n, f in calls.items()] + [("split_l2_warm", calls["split"], False)]:
         for _ in range(max(args.warmup, 3)):
-            sink.add_(flush_buf.sum())
+            if flush:
+                sink.add_(flush_buf.sum())
             fn()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for k in range(K):
-            sink.add_(flush_buf.sum())
+            if flush:
+                sink.add_(flush_buf.sum())
             ev[k][0].record()
             fn()
             ev[k][1].record()
@@ -527,7 +537,8 @@ def run_cascade(args):
             "value": round(nbytes / (res["cascade"] * 1e-3) / 1e9, 1), "unit": "GB/s",
             "us_per_call": round(res["cascade"] * 1e3, 2),
             "frac_of_copy_peak": round(nbytes / (res["cascade"] * 1e-3) / 1e9 / peak, 4),
-            "plain_split_us": round(res["split"] * 1e3, 2), "steps": K,
+            "plain_split_us": round(res["split"] * 1e3, 2),
+            "plain_split_us_without_flush": round(res["split_l2_warm"] * 1e3, 2), "steps": K,
             "config": {"workload": cfg.name, "groups": len(pre), "shared_prefix_blocks": pre.tolist(),
                        "unique_bytes": nbytes, "logical_kv_bytes": int(np.sum(dec_lens)) * tok_bytes,
                        "l2": "flushed before every call"}}
