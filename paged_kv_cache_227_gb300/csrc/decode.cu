@@ -782,8 +782,12 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
         float st[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) st[c] = (acc[0][c] + acc[1][c]) + (acc[2][c] + acc[3][c]);
-        // ---- online softmax of columns g0, g0+1 over tokens r4, r4+8
+        // ---- online softmax of columns g0, g0+1 over tokens r4, r4+8.  Each
+        // lane checks its own scores against the running max; only when one
+        // of them exceeds it by more than 2^8 does the warp reduce the tile's
+        // column maxima and move the running max (rare after the first tile).
         float mx[2];
+        bool grow = false;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           // (rows past a column's last position; the cut can reach into the
@@ -792,11 +796,13 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
           st[c] = r4 < vt ? st[c] * P.qscale : -INFINITY;
           st[2 + c] = r4 + 8 < vt ? st[2 + c] * P.qscale : -INFINITY;
           mx[c] = fmaxf(st[c], st[2 + c]);
-#pragma unroll
-          for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
+          grow = grow || mx[c] > m_run[c] + kRescaleThreshold;
         }
-        const bool grow = mx[0] > m_run[0] + kRescaleThreshold || mx[1] > m_run[1] + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, grow)) {  // warp-uniform; rare after the first tile
+        if (__any_sync(0xffffffffu, grow)) {  // warp-uniform
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
           float alpha[2];
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
