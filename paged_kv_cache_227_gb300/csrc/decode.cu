@@ -58,6 +58,11 @@ namespace pa {
 constexpr int kMaxSplitSeqs = 4096;  // sequences per split launch (prefix in shared memory)
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kLeanMinBlocks = 4;    // smallest LEAN range per warp
+// LEAN balances cost, not tiles: each (sequence, kv head) segment counts
+// kLeanPieceCost extra units ahead of its tiles, the measured cost of
+// starting a piece (its q, table window and record) in tile-equivalents, so
+// a warp whose range crosses several short segments gets fewer tiles.
+constexpr int kLeanPieceCost = 3;
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -98,6 +103,7 @@ struct Params {
   int sched;
   int partition_blocks;     // PARTITION: tiles per partition
   int lean_units;           // LEAN: number of warps the ranges are cut for
+  int lean_cost;            // LEAN: units counted ahead of each segment's tiles
   long long wait_limit_ns;
 };
 
@@ -325,12 +331,13 @@ struct Piece {
 
 struct PieceIter {
   const Params& P;
-  const int* pfx;   // shared: exclusive prefix over sequences (LEAN: tiles, PARTITION: partitions)
+  const int* pfx;   // shared: exclusive prefix over sequences (LEAN: units = tiles + lean_cost per
+                    // segment, PARTITION: partitions)
   const int* lens;  // shared: clamped lengths (split schedules), or null (read from P.seq_lens)
   int unit, n_units;
   long long x, x_end;        // SEGMENT / PARTITION cursor
-  long long cur, end;        // LEAN cursor
-  int li, lh, lj;
+  long long cur, end;        // LEAN cursor (units)
+  int li, lh;
   bool first;
 
   __device__ PieceIter(const Params& p, const int* prefix, const int* lengths, int u, int nu)
@@ -349,10 +356,8 @@ struct PieceIter {
           if (static_cast<long long>(P.Hkv) * pfx[mid] <= cur) lo = mid; else hi = mid - 1;
         }
         li = lo;
-        int nb = pfx[li + 1] - pfx[li];
-        long long off = cur - static_cast<long long>(P.Hkv) * pfx[li];
-        lh = static_cast<int>(off / nb);
-        lj = static_cast<int>(off - static_cast<long long>(lh) * nb);
+        const int cnt = pfx[li + 1] - pfx[li];
+        lh = static_cast<int>((cur - static_cast<long long>(P.Hkv) * pfx[li]) / cnt);
       }
     } else {
       x = unit;
@@ -366,27 +371,28 @@ struct PieceIter {
   __device__ bool next(Piece& pc) {
     if (P.sched == SCHED_LEAN) {
       if (cur >= end) return false;
-      int nb = pfx[li + 1] - pfx[li];
-      long long seg_start = static_cast<long long>(P.Hkv) * pfx[li] + static_cast<long long>(lh) * nb;
-      long long seg_end = seg_start + nb;
-      long long pend = end < seg_end ? end : seg_end;
+      // segment (li, lh): units [seg_start, seg_end), its tiles from rs on
+      const int cnt = pfx[li + 1] - pfx[li];
+      const long long seg_start = static_cast<long long>(P.Hkv) * pfx[li] + static_cast<long long>(lh) * cnt;
+      const long long rs = seg_start + P.lean_cost, seg_end = seg_start + cnt;
+      if (end <= rs) {  // the range ends before this segment's tiles
+        cur = end;
+        return false;
+      }
+      const long long from = cur > rs ? cur : rs;
+      const long long pend = end < seg_end ? end : seg_end;
       pc.i = li;
       pc.h = lh;
-      pc.j0 = lj;
-      pc.j1 = lj + static_cast<int>(pend - cur);
+      pc.j0 = static_cast<int>(from - rs);
+      pc.j1 = static_cast<int>(pend - rs);
       pc.L = len(li);
-      pc.final_out = (lj == 0 && pend == seg_end);
+      pc.final_out = (from == rs && pend == seg_end);
       pc.rec = 2ll * unit + (first ? 0 : 1);
       first = false;
       cur = pend;
-      if (cur == seg_end) {
-        lj = 0;
-        if (++lh == P.Hkv) {
-          lh = 0;
-          do { ++li; } while (li < P.B && pfx[li + 1] == pfx[li]);
-        }
-      } else {
-        lj = pc.j1;
+      if (cur == seg_end && ++lh == P.Hkv) {
+        lh = 0;
+        do { ++li; } while (li < P.B && pfx[li + 1] == pfx[li]);
       }
       return true;
     }
@@ -427,11 +433,13 @@ struct SegmentRecords {
   int count;
   __device__ SegmentRecords(const Params& P, const int* pfx, int i, int h) {
     if (P.sched == SCHED_LEAN) {
-      int nb = pfx[i + 1] - pfx[i];
+      const int cnt = pfx[i + 1] - pfx[i];
+      const int nb = cnt - P.lean_cost;
       per = lean_per(P, pfx);
-      s0 = static_cast<long long>(P.Hkv) * pfx[i] + static_cast<long long>(h) * nb;
-      c0 = s0 / per;
-      count = static_cast<int>((s0 + nb - 1) / per - c0 + 1);
+      s0 = static_cast<long long>(P.Hkv) * pfx[i] + static_cast<long long>(h) * cnt;  // segment's units start
+      const long long rs = s0 + P.lean_cost;                                          // its tiles start
+      c0 = rs / per;
+      count = static_cast<int>((rs + nb - 1) / per - c0 + 1);
       base = 0;
     } else {
       count = pfx[i + 1] - pfx[i];
@@ -440,6 +448,8 @@ struct SegmentRecords {
     }
   }
   __device__ long long at(const Params& P, int k) const {
+    // warp c0 holds an earlier piece (the previous segment's tiles end at
+    // s0) when its range starts before s0: then this is its second record
     if (P.sched == SCHED_LEAN) return 2 * (c0 + k) + ((k == 0 && s0 > c0 * per) ? 1 : 0);
     return base + static_cast<long long>(k) * P.Hkv;
   }
@@ -464,7 +474,8 @@ __device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report, 
       rows[P.B + i] = P.ext_ntok ? P.ext_ntok[i] : 1;
     }
     const int nb = (L + kBlock - 1) / kBlock;
-    pfx[i + 1] = P.sched == SCHED_LEAN ? nb : (nb + P.partition_blocks - 1) / P.partition_blocks;
+    pfx[i + 1] = P.sched == SCHED_LEAN ? (nb ? nb + P.lean_cost : 0)
+                                       : (nb + P.partition_blocks - 1) / P.partition_blocks;
   }
   __syncthreads();
   if (warp == 0) {
@@ -1651,6 +1662,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.sched = sched;
   P.partition_blocks = partition_blocks > 0 ? partition_blocks : 1;
   P.lean_units = 1;
+  P.lean_cost = kLeanPieceCost;
   P.wait_limit_ns = wait_limit_ns();
   cudaStream_t st = as_stream(stream);
   const bool bf16 = p->dtype == PA_BF16;
