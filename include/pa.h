@@ -277,6 +277,14 @@ int pa_copy_blocks(pa_pool_t pool, const int32_t* src, const int32_t* dst,
 int pa_profile_start(int capacity);
 int pa_profile_stop(float* ms, int cap);
 
+/* Failure-detection self-test (no counterpart on the pages): runs the
+ * kernels' bounded mbarrier wait, on `stream`, on a barrier nothing arrives
+ * at.  After limit_ns (0 < limit_ns <= 1e9) the wait gives up, records
+ * PA_ERR_TIMEOUT in the pool's error word (detail 9, the wait site) and the
+ * kernel returns; pa_check then reports it and the context stays usable.
+ * Nothing traps or hangs. */
+int pa_selftest_wait_timeout(pa_pool_t pool, long long limit_ns, void* stream);
+
 /* Synchronises `stream`, reads and clears the pool's device error word.
  * Returns PA_OK, PA_ERR_DEVICE_CHECK or PA_ERR_TIMEOUT; *detail (may be NULL)
  * receives the offending block id / slot (or the wait site for a timeout). */

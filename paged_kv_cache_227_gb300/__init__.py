@@ -57,6 +57,7 @@ def _load():
         "pa_decode_cascade": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, vp, vp, i32, vp, i32, vp,
                                     ctypes.c_size_t, vp]),
         "pa_cascade_groups": (i32, [vp, i32, i32, vp, i32, vp, vp, vp, ctypes.POINTER(i32)]),
+        "pa_selftest_wait_timeout": (i32, [vp, ctypes.c_longlong, vp]),
         "pa_decode_split_static": (i32, [vp, vp, vp, i32, vp, i32, i32, f32, vp, i32, i32, vp]),
         "pa_copy_blocks": (i32, [vp, vp, vp, i32, vp]),
         "pa_check": (i32, [vp, vp, ctypes.POINTER(i64)]),
@@ -331,6 +332,13 @@ def pa_profile_stop(cap=1 << 20):
     if n < 0:
         _check(n, "pa_profile_stop")
     return buf[:min(n, cap)].tolist()
+
+
+def pa_selftest_wait_timeout(pool, limit_ns, stream=None):
+    """Runs the kernels' bounded wait on a barrier nothing arrives at; it gives
+    up after limit_ns and records PA_ERR_TIMEOUT (read it with pa_check).
+    Returns the launch status."""
+    return lib.pa_selftest_wait_timeout(pool.handle, int(limit_ns), _stream(stream))
 
 
 def pa_check(pool, stream=None):

@@ -1463,6 +1463,19 @@ __global__ void cascade_combine(CascadeArgs A, const float* o_v, const float* ls
   store_out4(out, wid * kHeadDim + 4 * lane, r.x, r.y, r.z, r.w, out_dtype);
 }
 
+// Failure detection without a fault: the decode's bounded mbarrier wait on a
+// barrier that nothing arrives at.  After limit_ns it records PA_ERR_TIMEOUT
+// (detail: site 9) and returns; no copy is in flight, nothing traps.
+__global__ void wait_selftest_kernel(long long limit_ns, long long* err) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_addr(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  wait_phase(smem_addr(&bar), 0u, &abort_flag, limit_ns, err, 9);
+}
+
 // ---------------------------------------------------------------------------
 // Host side: dispatch over (G, dtype, fused).
 // ---------------------------------------------------------------------------
@@ -1940,6 +1953,12 @@ int pa_decode_cascade(pa_pool_t p, const void* q, const int32_t* block_tables, i
   const long long warps = static_cast<long long>(num_seqs) * n_q_heads;
   cascade_combine<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(A, o_v, lse_v, o_s, lse_s, out,
                                                                                    out_dtype);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_selftest_wait_timeout(pa_pool_t p, long long limit_ns, void* stream) {
+  if (!p || limit_ns <= 0 || limit_ns > 1000000000ll) return PA_ERR_INVALID;
+  wait_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(limit_ns, p->err);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
