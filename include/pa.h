@@ -82,7 +82,8 @@ size_t pa_pool_bytes(int num_blocks, int block_size, int n_kv_heads, int d_head,
 /* Allocates K and V pools (cudaMalloc on the current device, zero-filled) and
  * the device error word.  dtype is PA_FP16 or PA_BF16.  *out receives the
  * handle.  Errors: INVALID (num_blocks <= 0, n_kv_heads <= 0, out null),
- * UNSUPPORTED (block_size != 16, d_head != 128, dtype not 16-bit), OOM. */
+ * UNSUPPORTED (block_size != 16, d_head != 128, dtype not 16-bit, or
+ * num_blocks * n_kv_heads * 16 >= 2^31 token rows: a 512 GiB array), OOM. */
 int pa_pool_create(int num_blocks, int block_size, int n_kv_heads, int d_head,
                    int dtype, pa_pool_t* out);
 

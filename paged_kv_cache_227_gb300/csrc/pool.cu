@@ -97,6 +97,8 @@ int pa_pool_create(int num_blocks, int block_size, int n_kv_heads, int d_head, i
   if (!out || num_blocks <= 0 || n_kv_heads <= 0) return PA_ERR_INVALID;
   if (block_size != kBlock || d_head != kHeadDim) return PA_ERR_UNSUPPORTED;
   if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  // kernels address token rows (block * heads + head) * 16 with 32-bit ints
+  if (static_cast<long long>(num_blocks) * n_kv_heads * kBlock > 0x7fffffffll) return PA_ERR_UNSUPPORTED;
   *out = nullptr;
   pa_pool* p = new pa_pool();
   p->num_blocks = num_blocks;

@@ -54,6 +54,8 @@ def test_host_side_validation_needs_no_gpu(lib):
     assert pa.lib.pa_pool_create(0, 16, 2, 128, 1, ctypes.byref(h)) == pa.PA_ERR_INVALID
     assert pa.lib.pa_pool_create(4, 32, 2, 128, 1, ctypes.byref(h)) == pa.PA_ERR_UNSUPPORTED
     assert pa.lib.pa_pool_create(4, 16, 2, 96, 1, ctypes.byref(h)) == pa.PA_ERR_UNSUPPORTED
+    # 2^24 blocks x 8 heads x 16 rows = 2^31 token rows: past 32-bit row indices
+    assert pa.lib.pa_pool_create(1 << 24, 16, 8, 128, 1, ctypes.byref(h)) == pa.PA_ERR_UNSUPPORTED
     assert pa.lib.pa_decode(None, None, None, 1, None, 1, 8, 1.0, None, 2, None) == pa.PA_ERR_INVALID
     assert pa.lib.pa_cache_append(None, None, None, None, 1, None) == pa.PA_ERR_INVALID
     assert pa.strerror(pa.PA_ERR_TIMEOUT).startswith("a bounded")

@@ -201,6 +201,37 @@ def test_block_permutation_gives_bit_identical_output(pa):
     assert torch.equal(out1, out2)
 
 
+def test_block_ids_past_4_GiB_offsets(pa):
+    """The same sequences placed in the top blocks of a 140,000-block pool
+    (4.6 GB per K or V array, so byte offsets pass 2^32): the cache write puts
+    the new rows at the same bits, the block copy moves whole blocks, and every
+    decode path gives bit-identical output to the small pool's."""
+    c = GpuCase(3, lens=[33, 700, 5, 1200, 64])
+    ref = c.reference(after_append=True)
+    small = {m: _run(pa, c, m, c.pool()) for m in ("fused", "split", "segment")}
+    assert_close(small["split"], ref, "small pool")
+    n_big = 140_000
+    top = (n_big - 1 - np.arange(c.case.num_blocks)).astype(np.int64)   # block b -> n_big-1-b
+    big_k, big_v = c.kp, c.vp
+    k_ref, v_ref = c.appended_pools()          # the small pool after the append
+    c.tables = np.where(c.tables >= 0, top[np.maximum(c.tables, 0)], -1).astype(np.int32)
+    c.slots = top[c.slots // 16] * 16 + c.slots % 16
+    for m in ("fused", "split", "segment"):
+        pool = pa.Pool(n_big, c.cfg.n_kv_heads, c.dtype)
+        idx = torch.from_numpy(top).cuda()
+        pool.k[idx] = from_bits(big_k, c.dtype)
+        pool.v[idx] = from_bits(big_v, c.dtype)
+        out = _run(pa, c, m, pool)
+        assert torch.equal(out, small[m]), m
+        assert np.array_equal(bits(pool.k[idx]), k_ref) and np.array_equal(bits(pool.v[idx]), v_ref)
+    src = torch.tensor([n_big - 1, n_big - 5], dtype=torch.int32, device="cuda")
+    dst = torch.tensor([3, n_big - 2000], dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(pool, src, dst)
+    _check_ok(pa, pool)
+    assert torch.equal(pool.k[dst.long()], pool.k[src.long()]) and torch.equal(pool.v[dst.long()], pool.v[src.long()])
+    del pool
+
+
 def unshare(c):
     """Host side of the shared-prefix test: every sequence after the first gets
     private copies (appended to the pool) of the blocks it shares."""
