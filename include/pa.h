@@ -216,7 +216,8 @@ int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n
  * member's query heads over the shared blocks as one segment per (group, kv
  * head); a second attends each sequence over its blocks after its group's
  * prefix (all of them for a sequence in no group); a third merges the two by
- * log-sum-exp.  A group that breaks these rules is reported
+ * log-sum-exp.  The first pass runs on the SMs that the second's tail frees
+ * (a programmatic dependent launch), so the two passes overlap.  A group that breaks these rules is reported
  * (PA_ERR_DEVICE_CHECK) and its members are decoded without it.  q, out,
  * block_tables, seq_lens as for pa_decode; num_seqs and n_groups <= 4096.
  * workspace: device, >= pa_decode_cascade_workspace_bytes(...), 256-byte

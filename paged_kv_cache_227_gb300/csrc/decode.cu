@@ -105,7 +105,15 @@ struct Params {
   int lean_units;           // LEAN: number of warps the ranges are cut for
   int lean_cost;            // LEAN: units counted ahead of each segment's tiles
   long long wait_limit_ns;
+  int launch_flags;         // kLaunch* (host side; kLaunchSecondary also read by the kernel)
 };
+
+// Launch variants of one decode call (host side).  Secondary: the decode is
+// the programmatic dependent of the kernel before it in the stream, needs
+// nothing that kernel writes, and completes only after it (one thread waits
+// for it at the end), so the merge that depends on this decode also sees
+// that kernel's writes.  NoMerge / MergeOnly: launch one of the two kernels.
+constexpr int kLaunchSecondary = 1, kLaunchNoMerge = 2, kLaunchMergeOnly = 4;
 
 // Partial record of one piece: o[G][128], then m[g] at G*128+g and l[g] at
 // G*128+64+g (fp32; m in log2 units of the scaled scores).
@@ -1108,8 +1116,10 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     if (have_pc) load_q();
   }
 
-  // fused step: this grid completes only after the append grid
-  if (kFused && blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // fused step: this grid completes only after the append grid (secondary
+  // launch: after the kernel it depends on)
+  if ((kFused || (kExt && (P.launch_flags & kLaunchSecondary))) && blockIdx.x == 0 && threadIdx.x == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // --- drain: never leave a bulk copy in flight into this warp's ring -------
   if (!ok && lane == 0) {
@@ -1356,59 +1366,61 @@ struct CascadeArgs {
   long long* err;
 };
 
-// One CTA per group: member slots, prefix lengths and offsets, and the
-// packed queries of the prefix pass (zero past the group's members).
+// One CTA per (group, kv head): every CTA checks the group; those of kv head
+// 0 write the member slots and the prefix lengths and offsets; each packs its
+// kv head's queries of the prefix pass (zero past the group's members).
 __global__ void cascade_prep_groups(CascadeArgs A) {
   __shared__ int s_bad;
+  __shared__ int s_mem[PA_MAX_GROUP];  // the members (at most 8 / G of them)
   const int k = blockIdx.x;
+  const int h = blockIdx.y;
   const int m0 = A.group_start[k], m1 = A.group_start[k + 1];
   const int S = m1 - m0;
   const int P = A.prefix_blocks[k];
   const int cap = A.max_blocks * kBlock;
-  if (threadIdx.x == 0) {
-    bool bad = S < 1 || S > A.SM || P < 0 || P > A.max_blocks;
-    for (int m = 0; !bad && m < S; ++m) {
-      const int i = A.members[m0 + m];
-      bad = i < 0 || i >= A.B || A.seq_lens[i] < P * kBlock || A.seq_lens[i] > cap;
-    }
-    s_bad = bad;
+  if (threadIdx.x == 0) s_bad = S < 1 || S > A.SM || P < 0 || P > A.max_blocks;
+  __syncthreads();
+  if (!s_bad && threadIdx.x < S) {  // one thread per member
+    const int i = A.members[m0 + threadIdx.x];
+    s_mem[threadIdx.x] = i;
+    if (i < 0 || i >= A.B || A.seq_lens[i] < P * kBlock || A.seq_lens[i] > cap) s_bad = 1;
   }
   __syncthreads();
   if (!s_bad) {  // the shared blocks must be the first member's
-    const int first = A.members[m0];
+    const long long first = static_cast<long long>(s_mem[0]) * A.max_blocks;
+#pragma unroll 4
     for (int x = threadIdx.x; x < S * P; x += blockDim.x) {
-      const int i = A.members[m0 + x / P];
-      if (A.tables[static_cast<long long>(i) * A.max_blocks + x % P] !=
-          A.tables[static_cast<long long>(first) * A.max_blocks + x % P])
-        s_bad = 1;
+      const int i = s_mem[x / P];
+      if (A.tables[static_cast<long long>(i) * A.max_blocks + x % P] != A.tables[first + x % P]) s_bad = 1;
     }
   }
   __syncthreads();
   if (s_bad) {  // reported; its members are decoded without the group
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && h == 0) {
       record_error(A.err, PA_ERR_DEVICE_CHECK, k);
       A.lens_v[k] = 0;
       A.offs_v[k] = 0;
     }
     return;
   }
-  if (threadIdx.x == 0) {
-    A.lens_v[k] = P * kBlock;
-    A.offs_v[k] = A.members[m0] * A.max_blocks;
+  if (h == 0) {
+    if (threadIdx.x == 0) {
+      A.lens_v[k] = P * kBlock;
+      A.offs_v[k] = s_mem[0] * A.max_blocks;
+    }
+    if (threadIdx.x < S) A.slot_of[s_mem[threadIdx.x]] = k * 8 + threadIdx.x;
   }
-  for (int m = threadIdx.x; m < S; m += blockDim.x) A.slot_of[A.members[m0 + m]] = k * 8 + m;
-  // packed queries: 16-byte vectors
+  // packed queries of kv head h: 16-byte vectors
   const int GC = A.SM * A.G;  // columns per kv head
-  const long long n_vec = static_cast<long long>(A.Hkv) * GC * (kHeadDim / 8);
+  const int n_vec = GC * (kHeadDim / 8);
   const uint4* q = reinterpret_cast<const uint4*>(A.q);
-  uint4* qv = reinterpret_cast<uint4*>(A.qv) + static_cast<long long>(k) * n_vec;
-  for (long long x = threadIdx.x; x < n_vec; x += blockDim.x) {
-    const int c = static_cast<int>(x / (kHeadDim / 8));
-    const int h = c / GC, col = c % GC, m = col / A.G, g = col % A.G;
-    const int w = static_cast<int>(x % (kHeadDim / 8));
+  uint4* qv = reinterpret_cast<uint4*>(A.qv) + (static_cast<long long>(k) * A.Hkv + h) * n_vec;
+  for (int x = threadIdx.x; x < n_vec; x += blockDim.x) {
+    const int col = x / (kHeadDim / 8), m = col / A.G, g = col % A.G;
+    const int w = x % (kHeadDim / 8);
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (m < S) {
-      const int i = A.members[m0 + m];
+      const int i = s_mem[m];
       v = q[((static_cast<long long>(i) * A.Hq + h * A.G + g) * kHeadDim) / 8 + w];
     }
     qv[x] = v;
@@ -1538,6 +1550,10 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   }
   if (grid < 1) grid = 1;
   P.lean_units = static_cast<int>(grid) * NW;
+  const bool secondary = kExt && (P.launch_flags & kLaunchSecondary);
+  const bool with_decode = !(P.launch_flags & kLaunchMergeOnly);
+  const bool with_merge = P.sched != SCHED_SEGMENT && !(P.launch_flags & kLaunchNoMerge);
+  if (kFused && !with_decode) return PA_ERR_INVALID;
   const bool timed = 2 * static_cast<size_t>(g_prof_next) < g_prof_events.size();
   if (timed && cudaEventRecord(g_prof_events[2 * g_prof_next], stream) != cudaSuccess) return PA_ERR_CUDA;
   if (kFused) {
@@ -1547,6 +1563,8 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
                                       P.num_blocks, P.err, device, P.k_new, P.v_new, P.tables, P.max_blocks,
                                       P.seq_lens, P.B, stream);
     if (rc != PA_OK) return rc;
+  }
+  if (with_decode && (kFused || secondary)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(Shape<G>::kThreads);
@@ -1558,11 +1576,11 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, decode_kernel<G, kBf16, kFused, kExt>, P) != cudaSuccess) return PA_ERR_CUDA;
-  } else {
+  } else if (with_decode) {
     decode_kernel<G, kBf16, kFused, kExt><<<static_cast<int>(grid), Shape<G>::kThreads, bytes, stream>>>(P);
   }
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  if (P.sched != SCHED_SEGMENT) {
+  if (with_merge) {
     // the merge of split segments, as a programmatic dependent launch
     constexpr long long kWarpsPerCta = kMergeThreads / 32;
     long long items = static_cast<long long>(P.B) * P.Hkv * G;
@@ -1631,7 +1649,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
                          int Hq, float scale, void* out, int out_dtype, int sched,
                          int partition_blocks, void* ws, size_t ws_bytes, void* stream,
                          const int32_t* table_offs = nullptr, float* lse = nullptr,
-                         const int32_t* ext_ntok = nullptr, int ext_g = 0) {
+                         const int32_t* ext_ntok = nullptr, int ext_g = 0, int launch_flags = 0) {
   if (!p || !q || !tables || !seq_lens || !out || B <= 0 || Hq <= 0 || max_blocks <= 0)
     return PA_ERR_INVALID;
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
@@ -1677,6 +1695,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.lean_units = 1;
   P.lean_cost = kLeanPieceCost;
   P.wait_limit_ns = wait_limit_ns();
+  P.launch_flags = launch_flags;
   cudaStream_t st = as_stream(stream);
   const bool bf16 = p->dtype == PA_BF16;
   {
@@ -1853,7 +1872,7 @@ int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
 
 // Shared-prefix decode: workspace pieces, each 256-byte aligned.
 struct CascadeLayout {
-  size_t qv, o_v, lse_v, lens_v, offs_v, o_s, lse_s, lens_s, offs_s, slot_of, rec, total;
+  size_t qv, o_v, lse_v, lens_v, offs_v, o_s, lse_s, lens_s, offs_s, slot_of, rec, rec_v, total;
 };
 static bool cascade_layout(const pa_pool* p, int B, int Hq, int max_blocks, int n_groups, CascadeLayout* L) {
   if (!p || B <= 0 || Hq <= 0 || n_groups < 0 || max_blocks <= 0 || Hq % p->n_kv_heads) return false;
@@ -1880,7 +1899,8 @@ static bool cascade_layout(const pa_pool* p, int B, int Hq, int max_blocks, int 
   L->lens_s = take(static_cast<size_t>(B) * 4);
   L->offs_s = take(static_cast<size_t>(B) * 4);
   L->slot_of = take(static_cast<size_t>(B) * 4);
-  L->rec = take(ra.total > rb.total ? ra.total : rb.total);
+  L->rec = take(rb.total);                    // the suffix pass's records
+  L->rec_v = n_groups > 0 ? take(ra.total) : off;  // the prefix pass's (both passes run at once)
   L->total = off;
   return true;
 }
@@ -1932,24 +1952,36 @@ int pa_decode_cascade(pa_pool_t p, const void* q, const int32_t* block_tables, i
   cudaStream_t st = as_stream(stream);
   if (cudaMemsetAsync(A.slot_of, 0xff, sizeof(int32_t) * static_cast<size_t>(num_seqs), st) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (n_groups > 0) cascade_prep_groups<<<n_groups, 256, 0, st>>>(A);
+  if (n_groups > 0) cascade_prep_groups<<<dim3(n_groups, p->n_kv_heads), 128, 0, st>>>(A);
   cascade_prep_seqs<<<(num_seqs + 255) / 256, 256, 0, st>>>(A);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  const size_t rec_bytes = L.total - L.rec;
   float* o_v = reinterpret_cast<float*>(ws + L.o_v);
   float* lse_v = reinterpret_cast<float*>(ws + L.lse_v);
   float* o_s = reinterpret_cast<float*>(ws + L.o_s);
   float* lse_s = reinterpret_cast<float*>(ws + L.lse_s);
+  const size_t rec_s_bytes = L.rec_v - L.rec, rec_v_bytes = L.total - L.rec_v;
+  // The suffix pass fills the GPU; the prefix pass is its programmatic
+  // dependent and takes the SMs its tail frees.  Then the two merges and the
+  // combine, in stream order.
+  auto suffix = [&](int flags) {
+    return decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, A.lens_s, num_seqs, n_q_heads,
+                         scale, o_s, PA_FP32, SCHED_LEAN, 0, ws + L.rec, rec_s_bytes, stream, A.offs_s, lse_s,
+                         nullptr, 0, flags);
+  };
+  auto prefix = [&](int flags) {
+    return decode_common(p, A.qv, nullptr, nullptr, block_tables, max_blocks_per_seq, A.lens_v, n_groups,
+                         p->n_kv_heads * A.SM * G, scale, o_v, PA_FP32, SCHED_LEAN, 0, ws + L.rec_v, rec_v_bytes,
+                         stream, A.offs_v, lse_v, nullptr, 0, flags);
+  };
   int rc;
   if (n_groups > 0) {
-    rc = decode_common(p, A.qv, nullptr, nullptr, block_tables, max_blocks_per_seq, A.lens_v, n_groups,
-                       p->n_kv_heads * A.SM * G, scale, o_v, PA_FP32, SCHED_LEAN, 0, ws + L.rec, rec_bytes, stream,
-                       A.offs_v, lse_v);
-    if (rc != PA_OK) return rc;
+    if ((rc = suffix(kLaunchNoMerge)) != PA_OK) return rc;
+    if ((rc = prefix(kLaunchSecondary | kLaunchNoMerge)) != PA_OK) return rc;
+    if ((rc = prefix(kLaunchMergeOnly)) != PA_OK) return rc;
+    if ((rc = suffix(kLaunchMergeOnly)) != PA_OK) return rc;
+  } else if ((rc = suffix(0)) != PA_OK) {
+    return rc;
   }
-  rc = decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, A.lens_s, num_seqs, n_q_heads, scale,
-                     o_s, PA_FP32, SCHED_LEAN, 0, ws + L.rec, rec_bytes, stream, A.offs_s, lse_s);
-  if (rc != PA_OK) return rc;
   const long long warps = static_cast<long long>(num_seqs) * n_q_heads;
   cascade_combine<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(A, o_v, lse_v, o_s, lse_s, out,
                                                                                    out_dtype);
