@@ -2,7 +2,9 @@
 is an exact rearrangement of attention, so the oracle is the plain definition.
 Covers the Llama-2-13B MHA workload with its 2,048-token shared prefix, GQA
 groups of two, members whose whole cache is the shared prefix, sequences in
-no group, no groups at all, and a group that breaks the rules."""
+no group, no groups at all, a group that breaks the rules, and repeated calls (the
+prefix pass overlaps the suffix pass as a dependent launch: every call must
+give the same bits)."""
 import numpy as np
 import pytest
 import torch
@@ -89,3 +91,25 @@ def test_a_group_that_shares_nothing_is_reported_and_ignored(pa):
         out, code, _ = cascade(pa, c, c.tables, c.dec_lens, groups=groups)
         assert code == pa.PA_ERR_DEVICE_CHECK
         assert_close(out, ref, "members decoded without their broken group")
+
+
+def test_repeated_calls_give_the_same_bits(pa):
+    """Back-to-back calls on one stream, with a plain decode between some of
+    them: the overlapped passes and their merges always see complete inputs."""
+    c = GpuCase(4, lens=[2100, 2500, 2048, 3000, 2200, 2600])
+    pool = c.pool()
+    q = c.dev("q")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    bt, sl = dev(c.tables), dev(c.dec_lens)
+    gs, mem, pre = (dev(x) for x in pa.cascade_groups(c.tables, c.dec_lens, c.cfg.n_q_heads, c.cfg.n_kv_heads))
+    outs = [torch.full(q.shape, float("nan"), device="cuda") for _ in range(12)]
+    plain = torch.empty(q.shape, device="cuda")
+    for k, out in enumerate(outs):
+        pa.pa_decode_cascade(pool, q, bt, sl, c.case.scale, out, gs, mem, pre)
+        if k % 3 == 1:
+            pa.pa_decode_split(pool, q, bt, sl, c.case.scale, plain)
+    torch.cuda.synchronize()
+    assert pa.pa_check(pool)[0] == pa.PA_OK
+    for out in outs[1:]:
+        assert torch.equal(out, outs[0])
+    assert_close(outs[0], reference(c, c.tables, c.dec_lens), "cascade, repeated")
