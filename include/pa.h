@@ -195,7 +195,8 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
  * split (G = n_q_heads / n_kv_heads), each column masked to its token's causal
  * prefix, so every K/V tile is read once per 8/G new tokens.  workspace:
  * device, >= pa_decode_multi_workspace_bytes(...) bytes, 256-byte aligned.
- * ceil(n_q / (8/G)) + num_seqs <= 4096 (else PA_ERR_UNSUPPORTED).  A
+ * ceil(n_q / (8/G)) + num_seqs <= 4096 (else PA_ERR_UNSUPPORTED);
+ * num_seqs * max_blocks_per_seq < 2^31 (else PA_ERR_INVALID).  A
  * sequence with T_i > L_i, or a length out of range, records
  * PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros. */
 size_t pa_decode_multi_workspace_bytes(pa_pool_t pool, int n_q, int num_seqs,
@@ -219,7 +220,8 @@ int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n
  * log-sum-exp.  The first pass runs on the SMs that the second's tail frees
  * (a programmatic dependent launch), so the two passes overlap.  A group that breaks these rules is reported
  * (PA_ERR_DEVICE_CHECK) and its members are decoded without it.  q, out,
- * block_tables, seq_lens as for pa_decode; num_seqs and n_groups <= 4096.
+ * block_tables, seq_lens as for pa_decode; num_seqs and n_groups <= 4096;
+ * num_seqs * max_blocks_per_seq < 2^31 (else PA_ERR_INVALID).
  * workspace: device, >= pa_decode_cascade_workspace_bytes(...), 256-byte
  * aligned. */
 size_t pa_decode_cascade_workspace_bytes(pa_pool_t pool, int num_seqs, int n_q_heads,

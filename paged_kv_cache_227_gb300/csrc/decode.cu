@@ -1789,6 +1789,8 @@ struct MultiLayout {
 };
 static bool multi_layout(const pa_pool* p, int n_q, int B, int Hq, int max_blocks, MultiLayout* L) {
   if (!p || n_q <= 0 || B <= 0 || Hq <= 0 || max_blocks <= 0 || Hq % p->n_kv_heads) return false;
+  // table rows are addressed by 32-bit element offsets
+  if (static_cast<long long>(B) * max_blocks > 0x7fffffffll) return false;
   const int G = Hq / p->n_kv_heads;
   if (G > PA_MAX_GROUP) return false;
   L->TC = PA_MAX_GROUP / G;
@@ -1876,6 +1878,8 @@ struct CascadeLayout {
 };
 static bool cascade_layout(const pa_pool* p, int B, int Hq, int max_blocks, int n_groups, CascadeLayout* L) {
   if (!p || B <= 0 || Hq <= 0 || n_groups < 0 || max_blocks <= 0 || Hq % p->n_kv_heads) return false;
+  // table rows are addressed by 32-bit element offsets
+  if (static_cast<long long>(B) * max_blocks > 0x7fffffffll) return false;
   const int G = Hq / p->n_kv_heads;
   if (G > PA_MAX_GROUP) return false;
   const int GC = (PA_MAX_GROUP / G) * G;

@@ -352,3 +352,7 @@ def test_host_side_errors(pa):
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(pa.PagedAttentionError):
         pa.pa_decode_split(pool, q, bt, sl, 0.1, out, workspace=small)
+    # table rows addressed by 32-bit element offsets: 4096 x 2^20 entries is refused
+    assert pa.lib.pa_decode_cascade_workspace_bytes(pool.handle, 4096, 12, 1 << 20, 1) == 0
+    assert pa.lib.pa_decode_multi_workspace_bytes(pool.handle, 4096, 4096, 12, 1 << 20) == 0
+    assert pa.lib.pa_decode_multi_workspace_bytes(pool.handle, 8, 4, 12, 64) > 0
