@@ -232,6 +232,28 @@ def test_block_ids_past_4_GiB_offsets(pa):
     del pool
 
 
+def test_largest_split_batch(pa):
+    """4,096 sequences (the split schedules' limit: their prefix lives in
+    shared memory) of 1 to 81 tokens after the append, on every path; one
+    sequence more is refused by the split schedules."""
+    from workloads import Config
+    cfg = Config(90, "max-batch-8q-2kv-bf16", 8, 2, "bf16", 4096, ("uniform", 0, 80))
+    c = GpuCase(cfg)
+    ref = c.reference(after_append=True)
+    for mode in ("fused", "split", "segment"):
+        assert_close(_run(pa, c, mode, c.pool()), ref, f"batch 4096 {mode}")
+    pool = pa.Pool(4, 2, torch.bfloat16)
+    q = torch.zeros(4097, 8, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(4097, 8, 128, device="cuda")
+    bt = torch.full((4097, 1), -1, dtype=torch.int32, device="cuda")
+    sl = torch.zeros(4097, dtype=torch.int32, device="cuda")
+    with pytest.raises(pa.PagedAttentionError):
+        pa.pa_decode_split(pool, q, bt, sl, 0.1, out)
+    pa.pa_decode(pool, q, bt, sl, 0.1, out)          # the segment schedule has no such limit
+    _check_ok(pa, pool)
+    assert (out == 0).all()
+
+
 def unshare(c):
     """Host side of the shared-prefix test: every sequence after the first gets
     private copies (appended to the pool) of the blocks it shares."""
