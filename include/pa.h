@@ -272,8 +272,9 @@ int pa_copy_blocks(pa_pool_t pool, const int32_t* src, const int32_t* dst,
 /* Kernel timing for benchmarks.  pa_profile_start(capacity) creates
  * `capacity` pairs of CUDA events on the current device; each later
  * pa_decode / pa_decode_split / pa_append_decode call (until `capacity` calls
- * have been recorded) records one pair on its stream, right before and right
- * after its main decode kernel, so a merge kernel is outside the pair.
+ * have been recorded) records one pair on its stream, right before its first
+ * kernel and right after its last (the append kernel of the fused step, the
+ * decode kernel and the merge kernel).
  * pa_profile_stop(ms, cap) waits for the recorded pairs, writes up to cap
  * elapsed times in milliseconds to ms (host), releases the events and returns
  * how many pairs were recorded (or a negative status).  Process-wide, not

@@ -565,7 +565,8 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   // (kExt: per-sequence table offsets and log2-sum-exp outputs)
   int* const S_rows = kExt ? S.pfx + 2 * P.B + 1 : nullptr;
   if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0, S_rows);
-  // the merge kernel that follows may start its own set-up now
+  // a dependent launch that follows (the merge kernel, or the prefix pass
+  // of a cascade) may start its own set-up now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // zero rows of empty sequences (split schedules; SEGMENT pieces write them)
@@ -1145,6 +1146,11 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
 // completed and its records are visible.
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 128;
+// record batch sizes of the merge loop, as a type (a generic lambda picks one)
+template <int N>
+struct RbTag {
+  static constexpr int value = N;
+};
 template <int G>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Params P) {
   extern __shared__ int mpfx[];  // [B + 1]
@@ -1153,7 +1159,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const int lane = threadIdx.x & 31;
   const long long wpb = kMergeThreads / 32;
   const long long n_items = static_cast<long long>(P.B) * P.Hkv * G;
-  constexpr int RB = 16;  // records whose o loads are in flight together
+  constexpr int RB = 16;  // records whose o loads are in flight together (4 for short lists)
   for (long long it = blockIdx.x * wpb + (threadIdx.x >> 5); it < n_items; it += gridDim.x * wpb) {
     const int g = static_cast<int>(it % G);
     const long long sh = it / G;
@@ -1173,42 +1179,49 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       const float mk = have ? mv : -INFINITY;
       const float lk = have ? lv : 0.f;
       float wk = 0.f;
-      for (int b0 = 0; b0 < cnt; b0 += RB) {
-        float4 ob[RB];
+      auto batch = [&](auto tag) {
+        constexpr int RBv = decltype(tag)::value;
+        for (int b0 = 0; b0 < cnt; b0 += RBv) {
+          float4 ob[RBv];
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          const int k = b0 + r < cnt ? b0 + r : 0;
-          ob[r] = __ldcg(reinterpret_cast<const float4*>(P.ws + recs.at(P, c0 + k) * record_floats(G) +
-                                                         g * kHeadDim) + lane);
-        }
-        if (b0 == 0) {  // this chunk's weights; rescale what came before
-          float mx = mk;
+          for (int r = 0; r < RBv; ++r) {
+            const int k = b0 + r < cnt ? b0 + r : 0;
+            ob[r] = __ldcg(reinterpret_cast<const float4*>(P.ws + recs.at(P, c0 + k) * record_floats(G) +
+                                                           g * kHeadDim) + lane);
+          }
+          if (b0 == 0) {  // this chunk's weights; rescale what came before
+            float mx = mk;
 #pragma unroll
-          for (int msk = 1; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
-          const float mn = fmaxf(M, mx);
-          const float a = fast_exp2(M - mn);
-          wk = fast_exp2(mk - mn);
-          float lw = wk * lk;
+            for (int msk = 1; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+            const float mn = fmaxf(M, mx);
+            const float a = fast_exp2(M - mn);
+            wk = fast_exp2(mk - mn);
+            float lw = wk * lk;
 #pragma unroll
-          for (int msk = 1; msk < 32; msk <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, msk);
-          Ls = Ls * a + lw;
-          O.x *= a;
-          O.y *= a;
-          O.z *= a;
-          O.w *= a;
-          M = mn;
-        }
+            for (int msk = 1; msk < 32; msk <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, msk);
+            Ls = Ls * a + lw;
+            O.x *= a;
+            O.y *= a;
+            O.z *= a;
+            O.w *= a;
+            M = mn;
+          }
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          const float w = __shfl_sync(0xffffffffu, wk, (b0 + r) & 31);
-          if (b0 + r < cnt) {
-            O.x = fmaf(w, ob[r].x, O.x);
-            O.y = fmaf(w, ob[r].y, O.y);
-            O.z = fmaf(w, ob[r].z, O.z);
-            O.w = fmaf(w, ob[r].w, O.w);
+          for (int r = 0; r < RBv; ++r) {
+            const float w = __shfl_sync(0xffffffffu, wk, (b0 + r) & 31);
+            if (b0 + r < cnt) {
+              O.x = fmaf(w, ob[r].x, O.x);
+              O.y = fmaf(w, ob[r].y, O.y);
+              O.z = fmaf(w, ob[r].z, O.z);
+              O.w = fmaf(w, ob[r].w, O.w);
+            }
           }
         }
-      }
+      };
+      if (cnt <= 4)
+        batch(RbTag<4>{});
+      else
+        batch(RbTag<RB>{});
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
     const long long idx = (static_cast<long long>(i) * P.Hq + h * G + g) * kHeadDim + 4 * lane;
