@@ -156,14 +156,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// L2 policy for the K/V stream: evict first, so that the tiles, read once,
+// do not push out what is read again (q rows, tables, the partial records
+// the merge kernel reads back).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 // TMA tensor load of the 4-D box at (0, y, 0, 0) into shared memory: one
-// (block, head) tile of K and of V.
-__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap* map, int y, uint32_t bar) {
+// (block, head) tile of K and of V, with L2 cache policy `pol`.
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap* map, int y, uint32_t bar,
+                                              uint64_t pol) {
   const int z = 0;
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(z), "r"(y), "r"(z), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(z), "r"(y), "r"(z), "r"(z), "r"(bar), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -615,6 +624,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   // first of the next piece) is already being loaded, so an issue never waits
   // on the table.  Entering a piece also prefetches the piece after it's q
   // rows (and new K/V rows) into L2.
+  const uint64_t kv_policy = evict_first_policy();
   PieceIter iss(P, S.pfx, S_lens, unit, n_units);
   Piece ip, inx;  // current and next piece of the issue side
   bool ihave = iss.next(ip);
@@ -675,7 +685,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       if (valid) {
         mbar_arrive_expect_tx(fb, kStageBytes);
         const int y = (blk * P.Hkv + ip.h) * kBlock;  // first token row of the tile
-        tma_load_tile(ring_addr + stage * kStageBytes, &P.tmap_kv, y, fb);
+        tma_load_tile(ring_addr + stage * kStageBytes, &P.tmap_kv, y, fb, kv_policy);
       } else {
         record_error(P.err, PA_ERR_DEVICE_CHECK, static_cast<long long>(blk));
         mbar_arrive(fb);
