@@ -340,6 +340,12 @@ class OracleSample:
         seq = np.arange(n) // self.cfg.n_kv_heads
         return int(np.sum(self.lens[seq])) * self.cfg.d_head * 2 * 2
 
+    def outputs(self, n):
+        """The oracle's output rows of the first n groups (fp64)."""
+        rows = np.arange(n * self.G, dtype=np.int32)
+        return self.oracle.paged_decode(self.q, self.kp, self.vp, self.code, self.tables, self.lens,
+                                        self.case.scale, rows=rows, threads=self.threads)
+
     def run(self, n, reps=1):
         """Time `reps` passes of the oracle over the first n groups."""
         rows = np.arange(n * self.G, dtype=np.int32)
@@ -366,6 +372,12 @@ class OracleSample:
         passes = f", {reps} passes" if reps > 1 else ""
         return (f"first {n} of {self.groups} (sequence, kv head) groups, {self.G} q heads each, "
                 f"{toks} token rows{passes}; fp64 C oracle, {self.threads} OpenMP threads")
+
+
+def thread_count_diff(a, b, n):
+    """Largest |difference| between two oracle samples' outputs on the first
+    n groups (0 when the thread count does not change the result)."""
+    return float(np.max(np.abs(a.outputs(n) - b.outputs(n))))
 
 
 def main():
@@ -455,6 +467,9 @@ def main():
         dt1 = one.run(n1, reps1)
         line["cpu_baseline"]["one_thread"] = {"value": round(one.bytes_of(n1) * reps1 / dt1 / 1e9, 4),
                                               "sample": one.describe(n1, reps1) + f", {dt1:.1f} s"}
+        # the oracle's result does not depend on its thread count
+        n_chk = min(n1, 4 * threads)
+        line["cpu_baseline"]["threads_max_abs_diff"] = thread_count_diff(smp, one, n_chk)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
