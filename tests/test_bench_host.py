@@ -35,10 +35,10 @@ def test_step_bytes_of_the_shared_prefix_workload():
     assert b["kv"] == (int(lens.sum()) - (children - 1) * cfg.shared_prefix) * per_tok
     assert b["total"] == b["kv"] + b["new_rows"] + b["q"] + b["out"] + b["tables"]
     # no sharing: the two counts agree
-    cfg3 = CONFIGS[1]
-    case = make_case(cfg3)
+    tiny = CONFIGS[1]
+    case = make_case(tiny)
     tables, _, _, lens = build_tables(case, ReferenceAllocator(case.num_blocks, 16, case.free_order))
-    b = bench.step_bytes(cfg3, lens, tables)
+    b = bench.step_bytes(tiny, lens, tables)
     assert b["kv"] == b["kv_logical"]
 
 
