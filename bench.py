@@ -15,6 +15,17 @@ step.  `e2e` repeats the measurement through the same public calls with the
 step's inputs copied from pinned host memory (one staging buffer, one copy)
 and the output copied back inside the timed region.
 
+`other_configs` carries the same measurement for the other workloads (the
+tiny and batch-32 Qwen2.5-1.5B layouts, the Llama-2-13B shared-prefix
+workload with its cascade, the long-context workload with the balanced split
+and with fixed partitions), and `parity` the comparison of the timed step's
+result (one extra call with fp32 output, same inputs and launch) with the fp64
+oracle on the whole workload.
+
+`--gpus N` without a launcher starts N ranks itself (one process per GPU,
+weak scaling: every rank decodes its own batch; NCCL only for the barrier and
+the max/sum over ranks).  Under a launcher, WORLD_SIZE must equal N.
+
 `--impl reference` times the fp64 CPU oracle instead (the only other arm this
 repository has), on a bounded sample of the same workload.
 """
@@ -54,6 +65,9 @@ def parse():
                     choices=["decode", "multi-query", "cascade", "prefix-cache", "utilisation"],
                     help="decode: the headline step; the others time the further rows (one JSON line each)")
     ap.add_argument("--new-tokens", type=int, default=4, help="multi-query: new tokens per sequence")
+    ap.add_argument("--no-other-configs", action="store_true", help="headline workload only")
+    ap.add_argument("--clock-window", type=float, default=0.3,
+                    help="seconds of untimed steps right after the timed ones, to sample clocks under load")
     return ap.parse_args()
 
 
@@ -118,7 +132,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -191,51 +205,87 @@ def build_inputs(cfg_key, rank, device):
     return pa, cfg, case, tables, slots, dec_lens
 
 
-def run_ours(args, rank, world, local):
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    pa, cfg, case, tables, slots, dec_lens = build_inputs(args.workload, rank, device)
+class Flush:
+    """L2 flush by READING a 2x-L2 buffer: the cache is left holding clean
+    lines, so the timed step pays no write-back of a flush's dirty lines."""
+
+    def __init__(self, device):
+        self.l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.buf = torch.ones(2 * self.l2 // 4, dtype=torch.float32, device=device)
+        self.sink = torch.zeros(1, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.sink.add_(self.buf.sum())
+
+
+def device_inputs(pa, cfg, case, tables, dec_lens, device):
     pool = pa.Pool(case.num_blocks, cfg.n_kv_heads, cfg.torch_dtype)
     pool.k.copy_(case.k_pool.to(device))
     pool.v.copy_(case.v_pool.to(device))
-    q = case.q.to(device)
-    k_new = case.k_new.to(device)
-    v_new = case.v_new.to(device)
-    bt = torch.from_numpy(tables).to(device)
-    sl = torch.from_numpy(dec_lens).to(device)
-    out = torch.empty(q.shape, dtype=cfg.torch_dtype, device=device)
-    ws = pa.workspace_for(pool, q, bt, args.partition_blocks)
-    nbytes = step_bytes(cfg, dec_lens, tables)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    # L2 flush by READING a 2x-L2 buffer: the cache is left holding clean
-    # lines, so the timed step pays no write-back of a flush's dirty lines
-    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
-    flush_sink = torch.zeros(1, dtype=torch.float32, device=device)
+    return dict(pool=pool, q=case.q.to(device), k_new=case.k_new.to(device), v_new=case.v_new.to(device),
+                bt=torch.from_numpy(tables).to(device), sl=torch.from_numpy(dec_lens).to(device))
 
-    class _Flush:
-        @staticmethod
-        def zero_():
-            flush_sink.add_(flush_buf.sum())
-    flush = _Flush()
-    stream = torch.cuda.current_stream()
 
-    # the step, with its ctypes arguments marshalled once
+def fused_step_fn(pa, d, case, out, partition_blocks, ws):
+    """The fused step with its ctypes arguments marshalled once."""
     import ctypes
+    stream = torch.cuda.current_stream()
     fn = pa.lib.pa_append_decode
-    argv = (pool.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_new.data_ptr()),
-            ctypes.c_void_p(v_new.data_ptr()), ctypes.c_void_p(bt.data_ptr()), bt.shape[1],
-            ctypes.c_void_p(sl.data_ptr()), q.shape[0], q.shape[1], float(case.scale),
-            ctypes.c_void_p(out.data_ptr()), pa._DTYPE_CODE[out.dtype], args.partition_blocks,
+    argv = (d["pool"].handle, ctypes.c_void_p(d["q"].data_ptr()), ctypes.c_void_p(d["k_new"].data_ptr()),
+            ctypes.c_void_p(d["v_new"].data_ptr()), ctypes.c_void_p(d["bt"].data_ptr()), d["bt"].shape[1],
+            ctypes.c_void_p(d["sl"].data_ptr()), d["q"].shape[0], d["q"].shape[1], float(case.scale),
+            ctypes.c_void_p(out.data_ptr()), pa._DTYPE_CODE[out.dtype], partition_blocks,
             ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
-    launches_per_step = 3  # the append, the decode (its dependent) and the merge of split segments
 
     def step():
         code = fn(*argv)
         if code != 0:
             raise pa.PagedAttentionError(code, "pa_append_decode")
+    return step
 
+
+def time_steps(step, flush, K, W, profile=None):
+    """W untimed then K timed calls of `step`, L2 flushed before each; CUDA
+    events around each call (and the library's own events around its
+    launches when `profile` is the package).  Returns µs lists."""
+    for _ in range(max(W, 3)):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if profile is not None:
+        profile.pa_profile_start(K)
+    torch.cuda.synchronize()
+    for k in range(K):
+        flush()
+        ev[k][0].record()
+        step()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    step_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    kern_us = [x * 1e3 for x in profile.pa_profile_stop(K)] if profile is not None else None
+    return step_us, kern_us
+
+
+def run_ours(args, rank, world, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    pa, cfg, case, tables, slots, dec_lens = build_inputs(args.workload, rank, device)
+    d = device_inputs(pa, cfg, case, tables, dec_lens, device)
+    pool, q = d["pool"], d["q"]
+    out = torch.empty(q.shape, dtype=cfg.torch_dtype, device=device)
+    ws = pa.workspace_for(pool, q, d["bt"], args.partition_blocks)
+    nbytes = step_bytes(cfg, dec_lens, tables)
+    flush = Flush(device)
+    step = fused_step_fn(pa, d, case, out, args.partition_blocks, ws)
+    launches_per_step = 3  # the append, the decode (its dependent) and the merge of split segments
+
+    # clocks are sampled from before the warm-up to the end of an untimed
+    # window of steps right after the timed ones (the timed region alone is
+    # shorter than the sampling period)
+    clocks = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     code, detail = pa.pa_check(pool)
@@ -247,21 +297,26 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
     t_wall = time.perf_counter()
     for k in range(K):
-        flush.zero_()
+        flush()
         ev[k][0].record()
         step()
         ev[k][1].record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
-    clock_info = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = pa.pa_profile_stop(K)
     assert len(kern_ms) == K, "every timed step must record its decode kernel"
+    t_win = time.perf_counter()
+    while time.perf_counter() - t_win < args.clock_window:
+        for _ in range(50):
+            flush()
+            step()
+        torch.cuda.synchronize()
+    clock_info = clocks.stop()
     mean_ms = float(np.mean(step_ms))
     kern_mean = float(np.mean(kern_ms))
     code, detail = pa.pa_check(pool)
@@ -290,7 +345,7 @@ def run_ours(args, rank, world, local):
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KE)]
     torch.cuda.synchronize()
     for k in range(KE):
-        flush.zero_()
+        flush()
         eev[k][0].record()
         stage_d.copy_(stage_h, non_blocking=True)
         pa.pa_append_decode(pool, q_e, kn_e, vn_e, bt_e, sl_e, case.scale, out,
@@ -300,6 +355,17 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
 
+    # the timed step's result: the last timed call's native output, and one
+    # more call with the same inputs and launch whose output is fp32 (the
+    # kernel's arithmetic before the final rounding), for the oracle leg
+    out_native = out.float().cpu().numpy()
+    out32 = torch.empty(q.shape, dtype=torch.float32, device=device)
+    pa.pa_append_decode(pool, q, d["k_new"], d["v_new"], d["bt"], d["sl"], case.scale, out32,
+                        partition_blocks=args.partition_blocks, workspace=ws)
+    out_fp32 = out32.cpu().numpy()
+    code, detail = pa.pa_check(pool)
+    assert code == 0, (pa.strerror(code), detail)
+
     (mean_ms, e2e_ms), total_bytes = reduce_over_ranks([mean_ms, e2e_ms], nbytes["total"], device)
     pool.close()
     return dict(cfg=cfg, case=case, dec_lens=dec_lens, tables=tables, nbytes=nbytes, total_bytes=total_bytes,
@@ -307,7 +373,84 @@ def run_ours(args, rank, world, local):
                 p10=float(np.percentile(step_ms, 10)), p90=float(np.percentile(step_ms, 90)),
                 median=float(np.median(step_ms)),
                 kern_ms=kern_mean, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, wall=wall, clocks=clock_info,
-                launches=launches_per_step * K, K=K, l2=l2)
+                launches=launches_per_step * K, K=K, l2=flush.l2, out_native=out_native, out_fp32=out_fp32)
+
+
+def measure_other_configs(args, device):
+    """The other workloads, each on its own inputs: the fused step (balanced
+    split) and, where the configuration asks for them, fixed partitions
+    (long context) and the shared-prefix cascade next to the plain split
+    (Llama-2-13B).  Each record keeps the fp32 outputs of one extra call for
+    the oracle leg.  K timed steps, L2 flushed before each."""
+    import paged_kv_cache_227_gb300 as pa
+    peak, _ = measured_peak()
+    K, W = max(args.steps, 20), max(args.warmup, 3)
+    flush = Flush(device)
+    res, keep = {}, {}
+    for key in (1, 2, 4, 5):
+        _, cfg, case, tables, slots, dec_lens = build_inputs(key, 0, device)
+        d = device_inputs(pa, cfg, case, tables, dec_lens, device)
+        nb = step_bytes(cfg, dec_lens, tables)
+        rec = {"workload": cfg.name, "bytes_per_step": nb["total"], "tokens_attended": int(np.sum(dec_lens))}
+        runs = [("balanced", 0)]
+        if key == 5:
+            longest = int(-(-int(np.max(dec_lens)) // 16))
+            runs += [(f"partitions_{P}", -(-longest // P)) for P in (8, 16, 32)]
+        outs = {}
+        for name, pb in runs:
+            out = torch.empty(d["q"].shape, dtype=cfg.torch_dtype, device=device)
+            ws = pa.workspace_for(d["pool"], d["q"], d["bt"], pb)
+            step = fused_step_fn(pa, d, case, out, pb, ws)
+            step_us, kern_us = time_steps(step, flush, K, W, profile=pa)
+            kern = float(np.mean(kern_us))
+            r = {"partition_blocks": pb, "us_per_step": round(float(np.mean(step_us)), 2),
+                 "us_per_step_median": round(float(np.median(step_us)), 2), "kernel_us": round(kern, 2),
+                 "kernel_gbs": round(nb["total"] / (kern * 1e-6) / 1e9, 1),
+                 "frac_of_copy_peak": round(nb["total"] / (kern * 1e-6) / 1e9 / peak, 4)}
+            if name.startswith("partitions"):
+                r["partitions_of_longest_sequence"] = int(name.split("_")[1])
+            out32 = torch.empty(d["q"].shape, dtype=torch.float32, device=device)
+            pa.pa_append_decode(d["pool"], d["q"], d["k_new"], d["v_new"], d["bt"], d["sl"], case.scale, out32,
+                                partition_blocks=pb, workspace=ws)
+            outs[name] = out32.cpu().numpy()
+            rec[name] = r
+        code, detail = pa.pa_check(d["pool"])
+        assert code == 0, (pa.strerror(code), detail)
+        if key == 4:
+            # shared prefix: the cascade against the plain balanced split,
+            # decode only (the fused steps above wrote the new tokens), L2
+            # flushed before each call
+            out = torch.empty(d["q"].shape, dtype=cfg.torch_dtype, device=device)
+            gs, mem, pre = pa.cascade_groups(tables, dec_lens, cfg.n_q_heads, cfg.n_kv_heads)
+            gs_d, mem_d, pre_d = (torch.from_numpy(x).to(device) for x in (gs, mem, pre))
+            ws_c = torch.empty(pa.lib.pa_decode_cascade_workspace_bytes(d["pool"].handle, len(dec_lens), cfg.n_q_heads,
+                                                                        tables.shape[1], len(pre)),
+                               dtype=torch.uint8, device=device)
+            ws_s = pa.workspace_for(d["pool"], d["q"], d["bt"], 0)
+            calls = {"cascade": lambda o: pa.pa_decode_cascade(d["pool"], d["q"], d["bt"], d["sl"], case.scale, o,
+                                                               gs_d, mem_d, pre_d, workspace=ws_c),
+                     "plain_split": lambda o: pa.pa_decode_split(d["pool"], d["q"], d["bt"], d["sl"], case.scale, o,
+                                                                 0, ws_s)}
+            dec_bytes = nb["total"] - nb["new_rows"]
+            for name, call in calls.items():
+                step_us, _ = time_steps(lambda: call(out), flush, K, W)
+                t = float(np.mean(step_us))
+                rec[name] = {"us_per_call": round(t, 2), "bytes": dec_bytes,
+                             "frac_of_copy_peak": round(dec_bytes / (t * 1e-6) / 1e9 / peak, 4),
+                             "note": "decode only (the new tokens are already in the pool); "
+                                     "bytes count shared blocks once"}
+                out32 = torch.empty(d["q"].shape, dtype=torch.float32, device=device)
+                call(out32)
+                outs[name] = out32.cpu().numpy()
+            rec["cascade"]["groups"] = len(pre)
+            code, detail = pa.pa_check(d["pool"])
+            assert code == 0, (pa.strerror(code), detail)
+        keep[key] = (cfg, case, tables, dec_lens, outs)
+        res[str(key)] = rec
+        d["pool"].close()
+        del d
+        torch.cuda.empty_cache()
+    return res, keep
 
 
 class OracleSample:
@@ -380,15 +523,137 @@ def thread_count_diff(a, b, n):
     return float(np.max(np.abs(a.outputs(n) - b.outputs(n))))
 
 
+ABS_TOL, REL_TOL = 2e-3, 1e-2  # the parity bar on fp32 output (abs, relative to max |ref|)
+
+
+def parity_record(got32, ref, got_native=None, dtype=None, v_absmax=None):
+    """max |err| of the fp32 output against the fp64 oracle and the pass/fail
+    of the bar; for a native 16-bit output, how many elements lie more than
+    one 16-bit ulp (plus the kernel's own fp32 error floor) from the rounded
+    oracle value."""
+    got = np.asarray(got32, np.float64).reshape(ref.shape)
+    err = np.abs(got - ref)
+    bound = min(ABS_TOL, REL_TOL * float(np.abs(ref).max()))
+    rec = {"elements": int(ref.size), "max_abs_err": float(err.max()),
+           "max_rel_err": float(err.max() / max(float(np.abs(ref).max()), 1e-30)),
+           "tol_abs": ABS_TOL, "tol_rel": REL_TOL, "finite": bool(np.isfinite(got).all()),
+           "pass": bool(np.isfinite(got).all() and err.max() <= bound)}
+    if got_native is not None:
+        r16 = torch.from_numpy(ref).to(torch.float32).to(dtype).to(torch.float64).numpy()
+        mant = 7 if dtype == torch.bfloat16 else 10
+        min_exp = -126 if dtype == torch.bfloat16 else -14
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r16), 2.0 ** min_exp))) - mant)
+        floor = 2e-6 + 2.0 ** -18 * float(v_absmax)
+        excess = np.abs(np.asarray(got_native, np.float64).reshape(ref.shape) - r16) - (ulp + floor)
+        rec["native_16bit"] = {"max_abs_err": float(np.abs(np.asarray(got_native, np.float64).reshape(ref.shape) - ref).max()),
+                               "beyond_one_ulp": int((excess > 0).sum())}
+    return rec
+
+
+def oracle_reference(cfg, case, tables, dec_lens, threads, appended=True):
+    """The fp64 oracle's output for a whole workload: over the pool after the
+    step's cache write (fused step) or over the pool as cached."""
+    import oracle
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    kp, vp = bits(case.k_pool), bits(case.v_pool)
+    if appended:
+        kp, vp = oracle.cache.append(kp, vp, bits(case.k_new), bits(case.v_new), OracleSample._slots(tables, dec_lens))
+    return oracle.paged_decode(bits(case.q), kp, vp, 0 if cfg.dtype == "fp16" else 1, tables, dec_lens, case.scale,
+                               threads=threads)
+
+
+def oracle_leg(line, r, other, other_keep, args):
+    """Rank 0 at N=1 only: the fp64 oracle, as it stands, on the host's cores -
+    the CPU baseline (a bounded sample of the workload, ~10-30 s), and the
+    parity of every measured result against the oracle on its whole
+    workload."""
+    cfg = r["cfg"]
+    threads = len(os.sched_getaffinity(0))
+    smp = OracleSample(cfg, r["case"], r["tables"], r["dec_lens"], threads)
+    n, reps = smp.size_for(args.cpu_seconds)
+    dt = smp.run(n, reps)
+    line["cpu_baseline"] = {"value": round(smp.bytes_of(n) * reps / dt / 1e9, 4), "unit": "GB/s",
+                            "cores": threads, "kind": "oracle",
+                            "sample": smp.describe(n, reps) + f", {dt:.1f} s"}
+    # the same oracle on one thread, on a sample sized for about 3 s
+    one = OracleSample(cfg, r["case"], r["tables"], r["dec_lens"], 1)
+    n1, reps1 = one.size_for(3.0)
+    dt1 = one.run(n1, reps1)
+    line["cpu_baseline"]["one_thread"] = {"value": round(one.bytes_of(n1) * reps1 / dt1 / 1e9, 4),
+                                          "sample": one.describe(n1, reps1) + f", {dt1:.1f} s"}
+    # the oracle's result does not depend on its thread count
+    n_chk = min(n1, 4 * threads)
+    line["cpu_baseline"]["threads_max_abs_diff"] = thread_count_diff(smp, one, n_chk)
+
+    v_absmax = max(float(r["case"].v_pool.float().abs().max()), float(r["case"].v_new.float().abs().max()))
+    ref = oracle_reference(cfg, r["case"], r["tables"], r["dec_lens"], threads)
+    line["parity"] = parity_record(r["out_fp32"], ref, r["out_native"], cfg.torch_dtype, v_absmax)
+    line["parity"]["what"] = ("the timed step (same inputs and launch) with fp32 output vs the fp64 oracle on the whole "
+                              "workload; native_16bit: the last timed call's own output")
+    for key, (kcfg, kcase, ktables, klens, outs) in (other_keep or {}).items():
+        ref_app = oracle_reference(kcfg, kcase, ktables, klens, threads, appended=True)
+        for name, got in outs.items():  # (every call ran after the fused steps' cache write)
+            other[str(key)][name]["parity"] = parity_record(got, ref_app)
+
+
+def config_dict(cfg, case, dec_lens, tables, partition_blocks, l2_bytes):
+    """The workload description both arms print (identical for the same
+    workload)."""
+    nb = step_bytes(cfg, dec_lens, tables)
+    return {
+        "workload": cfg.name,
+        "batch_per_gpu": len(dec_lens),
+        "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "d_head": cfg.d_head,
+        "block_size": 16,
+        "lengths": "lognormal median 600 sigma 0.8 clip [16,8192] + 1 new token"
+        if cfg.key == 3 else str(cfg.lengths),
+        "tokens_attended": int(np.sum(dec_lens)),
+        "pool_blocks": case.num_blocks,
+        "step": "pa_append_decode (append, then balanced split-KV decode and LSE merge as dependent launches)",
+        "partition_blocks": partition_blocks,
+        "l2": f"flushed before every timed step (read of a {2 * l2_bytes >> 20} MiB buffer)",
+        "bytes_per_step": nb,
+    }
+
+
+GB300_L2_BYTES = 129 << 20  # L2 of the part, for the reference arm's config when no GPU is visible
+
+
+def spawn_ranks(args, n):
+    """Start n ranks of this program (one process per GPU) when no launcher
+    did; each sees RANK/LOCAL_RANK/WORLD_SIZE/MASTER_* like a torchrun rank."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    mp.start_processes(_rank_entry, args=(n, port, sys.argv[1:]), nprocs=n, start_method="spawn", join=True)
+
+
+def _rank_entry(rank, n, port, argv):
+    os.environ.update({"RANK": str(rank), "LOCAL_RANK": str(rank), "WORLD_SIZE": str(n),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.argv = [sys.argv[0]] + list(argv)
+    main()
+
+
 def main():
     args = parse()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return spawn_ranks(args, args.gpus)
     rank, world, local = dist_env()
-    if world > 1 and not torch.distributed.is_initialized():
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        torch.distributed.init_process_group(backend, device_id=torch.device("cuda", local)
-                                             if backend == "nccl" else None)
+    if world != args.gpus:
+        print(json.dumps({"error": f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU"}), flush=True)
+        sys.exit(2)
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if torch.cuda.device_count() <= local:
+        raise SystemExit(f"rank {rank}: needs cuda:{local}, only {torch.cuda.device_count()} GPU(s) visible")
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     if args.row != "decode":
         if rank == 0:
             print(json.dumps(ROWS[args.row](args)), flush=True)
@@ -399,6 +664,7 @@ def main():
     value = r["total_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
     achieved = nb["total"] / (r["kern_ms"] * 1e-3) / 1e9
     traffic = traffic_record(args.workload)
+    config = config_dict(cfg, r["case"], r["dec_lens"], r["tables"], args.partition_blocks, r["l2"])
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -415,22 +681,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else "fp16",
         "data": "synthetic (seeded N(0,1) q/k/v, lengths and random block placement; no dataset)",
-        "config": {
-            "workload": cfg.name,
-            "batch_per_gpu": len(r["dec_lens"]),
-            "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "d_head": cfg.d_head,
-            "block_size": 16,
-            "lengths": "lognormal median 600 sigma 0.8 clip [16,8192] + 1 new token"
-            if cfg.key == 3 else str(cfg.lengths),
-            "tokens_attended": int(np.sum(r["dec_lens"])),
-            "pool_blocks": r["case"].num_blocks,
-            "step": "pa_append_decode (append, then balanced split-KV decode and LSE merge as dependent launches)",
-            "partition_blocks": args.partition_blocks,
-            "l2": f"flushed before every timed step (read of a {2 * r['l2'] >> 20} MiB buffer)",
-            "bytes_per_step": nb,
-            "effective_gbs_logical": round(value * (nb["total"] - nb["kv"] + nb["kv_logical"]) / nb["total"], 1)
-            if nb["kv_logical"] != nb["kv"] else None,
-        },
+        "config": config,
         "roofline": {
             "bound": "hbm",
             "kernel": "append_tail_kernel + decode_kernel + merge_kernel (dependent launches), one step",
@@ -453,23 +704,14 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if nb["kv_logical"] != nb["kv"]:  # shared blocks: every sequence's own view of its bytes
+        line["effective_gbs_logical"] = round(value * (nb["total"] - nb["kv"] + nb["kv_logical"]) / nb["total"], 1)
+    other, other_keep = None, None
+    if rank == 0 and world == 1 and not args.no_other_configs:
+        other, other_keep = measure_other_configs(args, torch.device("cuda", local))
+        line["other_configs"] = other
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = len(os.sched_getaffinity(0))
-        smp = OracleSample(cfg, r["case"], r["tables"], r["dec_lens"], threads)
-        n, reps = smp.size_for(args.cpu_seconds)
-        dt = smp.run(n, reps)
-        line["cpu_baseline"] = {"value": round(smp.bytes_of(n) * reps / dt / 1e9, 4), "unit": "GB/s",
-                                "cores": threads, "kind": "oracle",
-                                "sample": smp.describe(n, reps) + f", {dt:.1f} s"}
-        # the same oracle on one thread, on a sample sized for about 3 s
-        one = OracleSample(cfg, r["case"], r["tables"], r["dec_lens"], 1)
-        n1, reps1 = one.size_for(3.0)
-        dt1 = one.run(n1, reps1)
-        line["cpu_baseline"]["one_thread"] = {"value": round(one.bytes_of(n1) * reps1 / dt1 / 1e9, 4),
-                                              "sample": one.describe(n1, reps1) + f", {dt1:.1f} s"}
-        # the oracle's result does not depend on its thread count
-        n_chk = min(n1, 4 * threads)
-        line["cpu_baseline"]["threads_max_abs_diff"] = thread_count_diff(smp, one, n_chk)
+        oracle_leg(line, r, other, other_keep, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -663,11 +905,13 @@ def run_reference(args, rank, world):
     dts = [smp.run(n, reps) for _ in range(args.steps)]
     dt = float(np.mean(dts)) if dts else smp.run(n, reps)
     value = smp.bytes_of(n) * reps / dt / 1e9
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size if torch.cuda.is_available() else GB300_L2_BYTES
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": {"workload": cfg.name, "sample": smp.describe(n, reps)},
+        "dtype": "f64", "data": "synthetic (seeded N(0,1) q/k/v, lengths and random block placement; no dataset)",
+        "config": config_dict(cfg, case, dec_lens, tables, args.partition_blocks, l2),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": smp.describe(n, reps)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -28,6 +28,12 @@
  *    returns.
  *  - Block size is 16 tokens and d_head is 128 (compile-time constants of the
  *    kernels); other values return PA_ERR_UNSUPPORTED.
+ *  - Calls that launch kernels run them on the current device, which must be
+ *    the device the pool was created on; a call made while another device
+ *    is current returns PA_ERR_INVALID before anything is launched.
+ *  - The library caches per-device state (SM counts, the static scratch
+ *    array's address) for the life of the process: do not use it again
+ *    after cudaDeviceReset.
  *  - Device-side bounds checks are always on: a block id outside
  *    [0, num_blocks) in a table or a slot outside [0, num_blocks*16) is never
  *    dereferenced.  The kernel skips it, records the first such event in the
@@ -157,7 +163,8 @@ size_t pa_decode_workspace_bytes(pa_pool_t pool, int num_seqs, int n_q_heads,
  * timing.  Pairs covered by a single unit are written directly.  workspace:
  * device, at least pa_decode_workspace_bytes(...) bytes, 16-byte aligned,
  * caller-owned; its contents on entry do not matter.  Calls that share a
- * workspace must not overlap on the GPU. */
+ * workspace must not overlap on the GPU.  num_seqs <= 4096 (the per-sequence
+ * prefix lives in shared memory), else PA_ERR_UNSUPPORTED. */
 int pa_decode_split(pa_pool_t pool, const void* q, const int32_t* block_tables,
                     int max_blocks_per_seq, const int32_t* seq_lens,
                     int num_seqs, int n_q_heads, float scale, void* out,
@@ -171,7 +178,10 @@ int pa_decode_split(pa_pool_t pool, const void* q, const int32_t* block_tables,
  * launched as its programmatic dependent, streams every other tile at once
  * and waits for the write only before a tile that holds a new token.  The
  * result equals pa_cache_append followed by pa_decode_split.  Rows with
- * L == 0 write nothing and output zeros. */
+ * L == 0 write nothing and output zeros.  num_seqs <= 4096, else
+ * PA_ERR_UNSUPPORTED.  Sequences that share a prefix are read once per
+ * sharer here; a caller that wants the shared blocks read once appends with
+ * pa_cache_append and decodes with pa_decode_cascade. */
 int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
                      const void* v_new, const int32_t* block_tables,
                      int max_blocks_per_seq, const int32_t* seq_lens,
@@ -242,7 +252,7 @@ int pa_decode_cascade(pa_pool_t pool, const void* q, const int32_t* block_tables
  * static device array owned by the library instead of a caller buffer.
  *  - Limit: the array holds PA_STATIC_SCRATCH_BYTES (12 MiB); a call whose
  *    pa_decode_workspace_bytes(...) exceeds it returns PA_ERR_SCRATCH_LIMIT
- *    before launching anything.  With partition_blocks == 0 this fits every
+ *    before launching anything.  num_seqs <= 4096, as for pa_decode_split.  With partition_blocks == 0 this fits every
  *    group size up to 8 on a 152-SM GPU; fixed partitions fit while
  *    num_seqs * n_kv_heads * ceil(max_blocks_per_seq / partition_blocks)
  *    records (each (G+1)*512 bytes) stay under the limit.
@@ -252,8 +262,9 @@ int pa_decode_cascade(pa_pool_t pool, const void* q, const int32_t* block_tables
  *    the first call on each device before any stream capture.
  *  - All calls share the array and it keeps the last call's contents;
  *    nothing in it needs to start at zero.  Calls that overlap on the GPU
- *    (two streams, or two devices' calls racing on one device's array) race
- *    on the array: serialise them.
+ *    (on two streams of one device) race on the array: serialise them.  A
+ *    call made while another device than the pool's is current is refused
+ *    (PA_ERR_INVALID), so a device's array is only used by its own pools.
  *  - No cudaMalloc, cudaFree or other allocating routine is called. */
 enum { PA_STATIC_SCRATCH_BYTES = 12 << 20 };
 int pa_decode_split_static(pa_pool_t pool, const void* q, const int32_t* block_tables,

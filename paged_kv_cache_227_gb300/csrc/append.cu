@@ -96,6 +96,7 @@ extern "C" int pa_cache_append(pa_pool_t p, const void* k_new, const void* v_new
                                const int64_t* slot_mapping, int n_tok, void* stream) {
   if (!p || n_tok < 0) return PA_ERR_INVALID;
   if (n_tok == 0) return PA_OK;
+  if (!on_pool_device(p)) return PA_ERR_INVALID;
   if (!k_new || !v_new || !slot_mapping) return PA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
     return PA_ERR_INVALID;  // rows are moved as 16-byte vectors

@@ -62,7 +62,7 @@ constexpr int kLeanMinBlocks = 4;    // smallest LEAN range per warp
 // kLeanPieceCost extra units ahead of its tiles, the measured cost of
 // starting a piece (its q, table window and record) in tile-equivalents, so
 // a warp whose range crosses several short segments gets fewer tiles.
-constexpr int kLeanPieceCost = 3;
+constexpr int kLeanPieceCost = 1;
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -331,8 +331,8 @@ __device__ __forceinline__ int clamp_len(const Params& P, int i) {
 }
 
 __device__ __forceinline__ long long lean_per(const Params& P, const int* pfx) {
-  long long T = static_cast<long long>(P.Hkv) * pfx[P.B];
-  long long per = (T + P.lean_units - 1) / P.lean_units;
+  const long long num = static_cast<long long>(P.Hkv) * pfx[P.B] + P.lean_units - 1;
+  const long long per = num < 0x7fffffffll ? static_cast<int>(num) / P.lean_units : num / P.lean_units;
   return per < kLeanMinBlocks ? kLeanMinBlocks : per;
 }
 
@@ -455,8 +455,14 @@ struct SegmentRecords {
       per = lean_per(P, pfx);
       s0 = static_cast<long long>(P.Hkv) * pfx[i] + static_cast<long long>(h) * cnt;  // segment's units start
       const long long rs = s0 + P.lean_cost;                                          // its tiles start
-      c0 = rs / per;
-      count = static_cast<int>((rs + nb - 1) / per - c0 + 1);
+      const long long last = rs + nb - 1;
+      if (last < 0x7fffffffll && per < 0x7fffffffll) {
+        c0 = static_cast<int>(rs) / static_cast<int>(per);
+        count = static_cast<int>(last) / static_cast<int>(per) - static_cast<int>(c0) + 1;
+      } else {
+        c0 = rs / per;
+        count = static_cast<int>(last / per - c0 + 1);
+      }
       base = 0;
     } else {
       count = pfx[i + 1] - pfx[i];
@@ -626,6 +632,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   // rows (and new K/V rows) into L2.
   const uint64_t kv_policy = evict_first_policy();
   PieceIter iss(P, S.pfx, S_lens, unit, n_units);
+  PieceIter cit = iss;  // the consumer walks the same list
   Piece ip, inx;  // current and next piece of the issue side
   bool ihave = iss.next(ip);
   bool inx_have = ihave && iss.next(inx);
@@ -695,7 +702,6 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     ++n_issued;
   };
   // ---- consume side -----------------------------------------------------------
-  PieceIter cit(P, S.pfx, S_lens, unit, n_units);
   Piece pc;
   bool have_pc = cit.next(pc);
   // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
@@ -1165,11 +1171,11 @@ template <int G>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Params P) {
   extern __shared__ int mpfx[];  // [B + 1]
   block_prefix(P, mpfx, nullptr, false);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long wpb = kMergeThreads / 32;
   const long long n_items = static_cast<long long>(P.B) * P.Hkv * G;
   constexpr int RB = 16;  // records whose o loads are in flight together (4 for short lists)
+  bool waited = false;
   for (long long it = blockIdx.x * wpb + (threadIdx.x >> 5); it < n_items; it += gridDim.x * wpb) {
     const int g = static_cast<int>(it % G);
     const long long sh = it / G;
@@ -1178,6 +1184,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     if (mpfx[i + 1] == mpfx[i]) continue;  // empty sequence: written by the decode kernel
     const SegmentRecords recs(P, mpfx, i, h);
     if (recs.count <= 1) continue;  // whole segment: written by the decode kernel
+    if (!waited) {  // the index math above needs only the lengths
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+    }
     float M = -INFINITY, Ls = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < recs.count; c0 += 32) {
@@ -1239,6 +1249,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     if (P.lse && lane == 0)
       P.lse[static_cast<long long>(i) * P.Hq + h * G + g] = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
   }
+  if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");  // completes after the decode grid
 }
 
 // ---------------------------------------------------------------------------
@@ -1684,6 +1695,7 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   if (fused && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15))
     return PA_ERR_INVALID;
   if ((table_offs || lse) && (sched == SCHED_SEGMENT || fused)) return PA_ERR_INVALID;
+  if (!on_pool_device(p)) return PA_ERR_INVALID;  // the kernels run on the current device
   WorkspaceLayout lay{};
   if (sched != SCHED_SEGMENT) {
     if (B > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
@@ -1854,6 +1866,7 @@ int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
     return PA_ERR_INVALID;
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PA_ERR_INVALID;
+  if (!on_pool_device(p)) return PA_ERR_INVALID;
   MultiLayout L{};
   if (!multi_layout(p, n_q, num_seqs, n_q_heads, max_blocks_per_seq, &L)) return PA_ERR_INVALID;
   if (num_seqs > kMaxSplitSeqs || L.Bv > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
@@ -1949,6 +1962,7 @@ int pa_decode_cascade(pa_pool_t p, const void* q, const int32_t* block_tables, i
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
   if (num_seqs > kMaxSplitSeqs || n_groups > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PA_ERR_INVALID;
+  if (!on_pool_device(p)) return PA_ERR_INVALID;
   CascadeLayout L{};
   if (!cascade_layout(p, num_seqs, n_q_heads, max_blocks_per_seq, n_groups, &L)) return PA_ERR_INVALID;
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
@@ -2016,7 +2030,7 @@ int pa_decode_cascade(pa_pool_t p, const void* q, const int32_t* block_tables, i
 }
 
 int pa_selftest_wait_timeout(pa_pool_t p, long long limit_ns, void* stream) {
-  if (!p || limit_ns <= 0 || limit_ns > 1000000000ll) return PA_ERR_INVALID;
+  if (!p || limit_ns <= 0 || limit_ns > 1000000000ll || !on_pool_device(p)) return PA_ERR_INVALID;
   wait_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(limit_ns, p->err);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -2031,8 +2045,10 @@ namespace pa {
 
 static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
 
-// Device address of g_static_scratch on `device` (the host-side symbol is
-// only a stand-in).  Looked up once per device with that device current.
+// Device address of g_static_scratch on the current device (the host-side
+// symbol is only a stand-in), looked up once per device and cached.  The
+// cache assumes that the device's context lives as long as the process:
+// after a cudaDeviceReset the library must not be used again.
 static int static_scratch_on(int device, void** out) {
   static std::mutex mu;
   static std::vector<void*> addr;
@@ -2040,13 +2056,8 @@ static int static_scratch_on(int device, void** out) {
   if (device < 0) return PA_ERR_INVALID;
   if (static_cast<size_t>(device) >= addr.size()) addr.resize(device + 1, nullptr);
   if (!addr[device]) {
-    int prev = -1;
-    if (cudaGetDevice(&prev) != cudaSuccess) return PA_ERR_CUDA;
-    if (prev != device && cudaSetDevice(device) != cudaSuccess) return PA_ERR_CUDA;
     void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-    if (prev != device) cudaSetDevice(prev);
-    if (e != cudaSuccess || !ptr) return PA_ERR_CUDA;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
     addr[device] = ptr;
   }
   *out = addr[device];
@@ -2060,6 +2071,8 @@ extern "C" int pa_decode_split_static(pa_pool_t p, const void* q, const int32_t*
                                       int n_q_heads, float scale, void* out, int out_dtype,
                                       int partition_blocks, void* stream) {
   if (!p || partition_blocks < 0) return PA_ERR_INVALID;
+  // the array looked up is the current device's: it must be the pool's
+  if (!on_pool_device(p)) return PA_ERR_INVALID;
   WorkspaceLayout lay{};
   if (!workspace_layout(p, num_seqs, n_q_heads, max_blocks_per_seq, partition_blocks, &lay))
     return PA_ERR_INVALID;

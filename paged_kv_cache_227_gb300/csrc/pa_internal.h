@@ -50,6 +50,17 @@ __device__ inline void record_error(long long* err, long long code, long long de
 // Number of SMs of the current device (cached per device).
 int sm_count(int device);
 
+// Entry check of every call that launches kernels: the current device must
+// be the pool's (kernels launch on the current device and address the pool's
+// memory, so a call from another device is refused before anything is
+// launched).  It also clears a pending non-sticky error of an earlier runtime
+// call, so that the launch checks that follow report this call's launches.
+inline bool on_pool_device(const pa_pool* p) {
+  (void)cudaGetLastError();
+  int cur = -1;
+  return cudaGetDevice(&cur) == cudaSuccess && cur == p->device;
+}
+
 // Wait limit for bounded in-kernel waits, in nanoseconds.
 long long wait_limit_ns();
 

@@ -54,7 +54,10 @@ int sm_count(int device) {
   if (static_cast<size_t>(device) >= cache.size()) cache.resize(device + 1, 0);
   if (cache[device] == 0) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      (void)cudaGetLastError();  // a failed query leaves no pending error behind
+      return 0;
+    }
     cache[device] = n;
   }
   return cache[device];
@@ -165,6 +168,7 @@ int pa_pool_shape(pa_pool_t p, int* num_blocks, int* n_kv_heads, int* d_head, in
 int pa_copy_blocks(pa_pool_t p, const int32_t* src, const int32_t* dst, int n, void* stream) {
   if (!p || n < 0 || (n > 0 && (!src || !dst))) return PA_ERR_INVALID;
   if (n == 0) return PA_OK;
+  if (!on_pool_device(p)) return PA_ERR_INVALID;
   int vec_per_block = p->n_kv_heads * kTileBytes / 16;
   copy_blocks_kernel<<<2 * n, 256, 0, as_stream(stream)>>>(
       static_cast<uint4*>(p->k), static_cast<uint4*>(p->v), src, dst, n, p->num_blocks,

@@ -49,3 +49,34 @@ def test_oracle_result_does_not_depend_on_threads():
     many = bench.OracleSample(cfg, case, tables, lens, 4)
     one = bench.OracleSample(cfg, case, tables, lens, 1)
     assert bench.thread_count_diff(many, one, many.groups) == 0.0
+
+
+def test_both_arms_describe_the_workload_identically():
+    cfg = CONFIGS[3]
+    case = make_case(cfg)
+    tables, _, _, lens = build_tables(case, ReferenceAllocator(case.num_blocks, 16, case.free_order))
+    a = bench.config_dict(cfg, case, lens, tables, 0, bench.GB300_L2_BYTES)
+    case2 = make_case(cfg)
+    tables2, _, _, lens2 = build_tables(case2, ReferenceAllocator(case2.num_blocks, 16, case2.free_order))
+    b = bench.config_dict(cfg, case2, lens2, tables2, 0, bench.GB300_L2_BYTES)
+    assert a == b
+    assert a["workload"] == cfg.name and a["tokens_attended"] == int(lens.sum())
+
+
+def test_parity_record_bar_and_native_check():
+    rng = np.random.default_rng(0)
+    ref = rng.standard_normal((4, 8, 128))
+    ok = bench.parity_record(ref + 1e-4, ref)
+    assert ok["pass"] and abs(ok["max_abs_err"] - 1e-4) < 1e-9
+    bad = bench.parity_record(ref + 3e-3, ref)
+    assert not bad["pass"]
+    nan = ref.copy()
+    nan[0, 0, 0] = np.nan
+    assert not bench.parity_record(nan, ref)["pass"]
+    import torch
+    rn = torch.from_numpy(ref).float().to(torch.bfloat16).double().numpy()
+    rec = bench.parity_record(ref, ref, got_native=rn, dtype=torch.bfloat16, v_absmax=4.0)
+    assert rec["native_16bit"]["beyond_one_ulp"] == 0
+    off = rn * (1 + 2.0 ** -5)  # four bf16 ulps off
+    rec = bench.parity_record(ref, ref, got_native=off, dtype=torch.bfloat16, v_absmax=4.0)
+    assert rec["native_16bit"]["beyond_one_ulp"] > 0
