@@ -203,12 +203,16 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
  * out: device [n_q][n_q_heads][128] in out_dtype.  A sequence's new tokens
  * are packed 8/G at a time into the columns of one segment of the balanced
  * split (G = n_q_heads / n_kv_heads), each column masked to its token's causal
- * prefix, so every K/V tile is read once per 8/G new tokens.  workspace:
- * device, >= pa_decode_multi_workspace_bytes(...) bytes, 256-byte aligned.
+ * prefix, so every K/V tile is read once per 8/G new tokens.  A planning
+ * kernel maps each packed column block to its query row; the decode (its
+ * programmatic dependent) and the merge read q and write out through that
+ * map.  workspace: device, >= pa_decode_multi_workspace_bytes(...) bytes,
+ * 256-byte aligned (lengths, maps and the split's partial records).
  * ceil(n_q / (8/G)) + num_seqs <= 4096 (else PA_ERR_UNSUPPORTED);
  * num_seqs * max_blocks_per_seq < 2^31 (else PA_ERR_INVALID).  A
  * sequence with T_i > L_i, or a length out of range, records
- * PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros. */
+ * PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros; rows that a q_start
+ * breaking its rules leaves to no sequence are not written. */
 size_t pa_decode_multi_workspace_bytes(pa_pool_t pool, int n_q, int num_seqs,
                                        int n_q_heads, int max_blocks_per_seq);
 int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n_q,

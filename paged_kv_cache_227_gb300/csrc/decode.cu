@@ -91,6 +91,10 @@ struct Params {
   float* lse;               // [B][Hq] log2-sum-exp of the scaled scores (log2 units), or null
   const int32_t* ext_ntok;  // [B]: query tokens packed in sequence i's columns, or null (1)
   int ext_g;                // columns per packed token (the real group size)
+  const int32_t* ext_qbase;  // [B]: q / out row of sequence i's first packed token (its ext_ntok[i]
+                             // tokens are the rows that follow), or -1 (none); null: q and out are
+                             // [B][Hq][128]
+  int ext_hq;                // with ext_qbase: heads of a q / out row ([rows][ext_hq][128])
   const int32_t* seq_lens;  // [B]
   void* out;                // [B][Hq][128]
   float* ws;                // partial records
@@ -113,11 +117,25 @@ struct Params {
 // nothing that kernel writes, and completes only after it (one thread waits
 // for it at the end), so the merge that depends on this decode also sees
 // that kernel's writes.  NoMerge / MergeOnly: launch one of the two kernels.
-constexpr int kLaunchSecondary = 1, kLaunchNoMerge = 2, kLaunchMergeOnly = 4;
+// AfterPlan: the decode is the programmatic dependent of a kernel that writes
+// its lengths, table offsets and row maps, and waits for it before reading them.
+constexpr int kLaunchSecondary = 1, kLaunchNoMerge = 2, kLaunchMergeOnly = 4, kLaunchAfterPlan = 8;
 
 // Partial record of one piece: o[G][128], then m[g] at G*128+g and l[g] at
 // G*128+64+g (fp32; m in log2 units of the scaled scores).
 __host__ __device__ constexpr int record_floats(int G) { return (G + 1) * 128; }
+// Columns of one segment of packed query tokens (two halves of the MMA's 8).
+constexpr int kMaxPackedCols = 16;
+
+// Element offset in q and out of column g of kv head h of a sequence whose
+// packed tokens are rows r0 .. r0 + nt - 1 (ext_g columns each), or -1 when
+// the column carries no query: column g is token g / ext_g's query head
+// h * ext_g + g % ext_g.
+__device__ __forceinline__ long long packed_io_offset(const Params& P, int r0, int nt, int h, int g) {
+  const int tt = g / P.ext_g;
+  if (r0 < 0 || tt >= nt) return -1;
+  return (static_cast<long long>(r0 + tt) * P.ext_hq + h * P.ext_g + (g - tt * P.ext_g)) * 128;
+}
 
 // ---------------------------------------------------------------------------
 // PTX helpers.
@@ -495,6 +513,7 @@ __device__ void block_prefix(const Params& P, int* pfx, int* lens, bool report, 
     if (rows) {
       rows[i] = P.table_offs[i];
       rows[P.B + i] = P.ext_ntok ? P.ext_ntok[i] : 1;
+      rows[2 * P.B + i] = P.ext_qbase ? P.ext_qbase[i] : -1;
     }
     const int nb = (L + kBlock - 1) / kBlock;
     pfx[i + 1] = P.sched == SCHED_LEAN ? (nb ? nb + P.lean_cost : 0)
@@ -544,14 +563,14 @@ constexpr bool smem_layout_ok() {
 }
 static_assert(smem_layout_ok<1>() && smem_layout_ok<2>() && smem_layout_ok<3>() &&
                   smem_layout_ok<4>() && smem_layout_ok<5>() && smem_layout_ok<6>() &&
-                  smem_layout_ok<7>() && smem_layout_ok<8>(),
+                  smem_layout_ok<7>() && smem_layout_ok<8>() && smem_layout_ok<16>(),
               "shared-memory layout breaks a swizzle, vector or mbarrier alignment");
 
 // Dynamic shared memory to request: the struct, the prefix array, and slack
 // to align the base to 1024 bytes.
 template <int G>
 constexpr size_t smem_bytes(int B, bool rows = false) {
-  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>((rows ? 4 : 2) * B + 1) + 1024;
+  return sizeof(Smem<G>) + sizeof(int) * static_cast<size_t>((rows ? 5 : 2) * B + 1) + 1024;
 }
 
 // ---------------------------------------------------------------------------
@@ -576,10 +595,17 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // tail of shared memory: prefix [B+1], lengths [B], table offsets [B]
-  // (kExt: per-sequence table offsets and log2-sum-exp outputs)
+  // tail of shared memory: prefix [B+1], lengths [B], and (kExt) per sequence
+  // its table offset [B], packed tokens [B] and first q / out row [B]
   int* const S_rows = kExt ? S.pfx + 2 * P.B + 1 : nullptr;
+  // (a planning kernel before this one writes the lengths and maps read here)
+  if (kExt && (P.launch_flags & kLaunchAfterPlan)) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (P.sched != SCHED_SEGMENT) block_prefix(P, S.pfx, S.pfx + P.B + 1, blockIdx.x == 0, S_rows);
+  // element offset of column g of kv head h of sequence i in q and out, or -1
+  auto io_at = [&](int i, int h, int g) -> long long {
+    if (kExt && P.ext_qbase) return packed_io_offset(P, S_rows[2 * P.B + i], S_rows[P.B + i], h, g);
+    return (static_cast<long long>(i) * P.Hq + h * G + g) * kHeadDim;
+  };
   // a dependent launch that follows (the merge kernel, or the prefix pass
   // of a cascade) may start its own set-up now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -588,8 +614,15 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   if (P.sched != SCHED_SEGMENT) {
     for (int i = blockIdx.x; i < P.B; i += gridDim.x) {
       if (S.pfx[i + 1] != S.pfx[i]) continue;
-      for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x)
-        store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
+      for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x) {
+        if constexpr (kExt) {
+          const int col = x / kHeadDim;
+          const long long at = io_at(i, col / G, col % G);
+          if (at >= 0) store_out(P.out, at + x % kHeadDim, 0.f, P.out_dtype);
+        } else {
+          store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
+        }
+      }
       if (kExt && P.lse)
         for (int x = threadIdx.x; x < P.Hq; x += blockDim.x) P.lse[static_cast<long long>(i) * P.Hq + x] = -INFINITY;
     }
@@ -620,6 +653,12 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   // faster than mode 2 for the plain decode of G = 6.
   constexpr int kPvMode = G <= 4 ? 1 : (kExt ? 2 : 0);
   constexpr bool kMmaPv = kPvMode != 0;
+  // Column halves: the extended kernel takes up to 16 columns as two groups
+  // of 8 (the MMA's n), which share each K/V tile, its wait and its operand
+  // loads.  kSc: independent score accumulators per half.
+  constexpr int NCH = G > 8 ? 2 : 1;
+  constexpr int kSc = NCH == 1 ? 4 : 2;
+  static_assert(G <= 8 || kPvMode == 2, "more than 8 columns only in the extended kernel");
   // value phase: lane owns 16-byte chunk c16 of the V rows of token parity r16
   const int c16 = lane & 15;
   const int r16 = lane >> 4;
@@ -646,8 +685,15 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     return jj < pp.j1 ? P.tables[off + jj] : 0;
   };
   auto prefetch_rows = [&](const Piece& pp) {
-    const long long qrow = (static_cast<long long>(pp.i) * P.Hq + pp.h * G) * kHeadDim;
-    if (lane < 2 * G) asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + qrow + 64 * lane));
+    if constexpr (kExt) {
+      if (lane < 2 * G) {
+        const long long at = io_at(pp.i, pp.h, lane >> 1);
+        if (at >= 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + at + 64 * (lane & 1)));
+      }
+    } else {
+      const long long qrow = (static_cast<long long>(pp.i) * P.Hq + pp.h * G) * kHeadDim;
+      if (lane < 2 * G) asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + qrow + 64 * lane));
+    }
   };
   auto load_following = [&]() {
     if (tb_base + 32 < ip.j1) {
@@ -704,20 +750,28 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   // ---- consume side -----------------------------------------------------------
   Piece pc;
   bool have_pc = cit.next(pc);
-  // B fragments of Q^T: column g = r4 of the group (zero past G), k = dims
-  uint32_t qb[8][2];
+  // B fragments of Q^T: column g = 8 hf + r4 of the group (zero past G), k = dims
+  uint32_t qb[NCH][8][2];
   auto load_q = [&]() {
-    if (r4 < G) {
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          P.q + (static_cast<long long>(pc.i) * P.Hq + pc.h * G + r4) * kHeadDim);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qb[ks][0] = qrow[8 * ks + c4];
-        qb[ks][1] = qrow[8 * ks + 4 + c4];
+    for (int hf = 0; hf < NCH; ++hf) {
+      const int col = 8 * hf + r4;
+      long long at;
+      if constexpr (kExt)
+        at = col < G ? io_at(pc.i, pc.h, col) : -1;
+      else
+        at = col < G ? (static_cast<long long>(pc.i) * P.Hq + pc.h * G + col) * kHeadDim : -1;
+      if (at >= 0) {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(P.q + at);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          qb[hf][ks][0] = qrow[8 * ks + c4];
+          qb[hf][ks][1] = qrow[8 * ks + 4 + c4];
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) qb[hf][ks][0] = qb[hf][ks][1] = 0u;
       }
-    } else {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
     }
   };
   if (have_pc) load_q();  // in flight while the first loads are issued
@@ -734,31 +788,46 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     // high halves and columns 4-7 the low halves of the weights of heads 0-3.
     // FMA path (G > 4): o[g][e] holds dims 8*c16+2e, +1 of head g over the
     // tokens of parity r16.
-    // Mode 2: oc holds the products with the high halves of all 8 columns
-    // (heads 2c4, 2c4+1 for this lane), oc2 those with the low halves.
-    float oc[kMmaPv ? 8 : 1][4];
-    float oc2[kPvMode == 2 ? 8 : 1][4];
+    // Mode 2: oc[hf] holds the products with the high halves of the 8
+    // columns of half hf (columns 8hf + 2c4, +1 for this lane), oc2 those
+    // with the low halves; with two halves both go into oc (registers).
+    constexpr bool kLoApart = kPvMode == 2 && NCH == 1;
+    float oc[NCH][kMmaPv ? 8 : 1][4];
+    float oc2[kLoApart ? 8 : 1][4];
     float2 o[kMmaPv ? 1 : G][4];
 #pragma unroll
-    for (int mt = 0; mt < (kMmaPv ? 8 : 1); ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+    for (int hf = 0; hf < NCH; ++hf)
 #pragma unroll
-    for (int mt = 0; mt < (kPvMode == 2 ? 8 : 1); ++mt) oc2[mt][0] = oc2[mt][1] = oc2[mt][2] = oc2[mt][3] = 0.f;
+      for (int mt = 0; mt < (kMmaPv ? 8 : 1); ++mt) oc[hf][mt][0] = oc[hf][mt][1] = oc[hf][mt][2] = oc[hf][mt][3] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < (kLoApart ? 8 : 1); ++mt) oc2[mt][0] = oc2[mt][1] = oc2[mt][2] = oc2[mt][3] = 0.f;
 #pragma unroll
     for (int g = 0; g < (kMmaPv ? 1 : G); ++g)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float m_run[NCH][2], l_run[NCH][2];
+#pragma unroll
+    for (int hf = 0; hf < NCH; ++hf) {
+      m_run[hf][0] = m_run[hf][1] = -INFINITY;
+      l_run[hf][0] = l_run[hf][1] = 0.f;
+    }
     const int nb_total = (pc.L + kBlock - 1) / kBlock;
-    // extended kernel: the sequence packs ntok query tokens, G / ntok columns
-    // each; token t of them sees ntok - 1 - t fewer positions (causal)
-    int cut0 = 0, cut1 = 0;
+    // extended kernel: the sequence packs ntok query tokens, ext_g columns
+    // each; token t of them sees ntok - 1 - t fewer positions (causal).
+    // cut[hf][c]: positions column 8hf + g0 + c does not see.
+    int cut[NCH][2];
+#pragma unroll
+    for (int hf = 0; hf < NCH; ++hf) cut[hf][0] = cut[hf][1] = 0;
     if constexpr (kExt) {
       const int nt = S_rows[P.B + pc.i];
       if (nt > 1) {
-        cut0 = nt - 1 - g0 / P.ext_g;
-        cut1 = nt - 1 - (g0 + 1) / P.ext_g;
-        cut0 = cut0 < 0 ? 0 : cut0;
-        cut1 = cut1 < 0 ? 0 : cut1;
+#pragma unroll
+        for (int hf = 0; hf < NCH; ++hf)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int x = nt - 1 - (8 * hf + g0 + c) / P.ext_g;
+            cut[hf][c] = x < 0 ? 0 : x;
+          }
       }
     }
 
@@ -787,20 +856,25 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       }
       return true;
     };
-    // S^T = K Q^T for the tile in stage s, in 4 independent accumulators
-    auto scores = [&](int s, float (&acc)[4][4]) {
+    // S^T = K Q^T for the tile in stage s, in kSc independent accumulators
+    // per half (each K fragment serves both halves)
+    auto scores = [&](int s, float (&acc)[NCH][kSc][4]) {
       const uint32_t ks_addr = ring_addr + s * kStageBytes;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+      for (int hf = 0; hf < NCH; ++hf)
+#pragma unroll
+        for (int c = 0; c < kSc; ++c) acc[hf][c][0] = acc[hf][c][1] = acc[hf][c][2] = acc[hf][c][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(ks_addr + swz(k_tok, 2 * ks + k_cadd), a0, a1, a2, a3);
-        mma16816<kBf16>(acc[ks & 3], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+#pragma unroll
+        for (int hf = 0; hf < NCH; ++hf)
+          mma16816<kBf16>(acc[hf][ks % kSc], a0, a1, a2, a3, qb[hf][ks][0], qb[hf][ks][1]);
       }
     };
 
-    float acc[4][4];
+    float acc[NCH][kSc][4];
     int cur_blk = -1;
     bool cur_touched = false;
     if (pc.j1 > pc.j0) {
@@ -813,92 +887,110 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       const int s = n % SW;
       const uint8_t* Vs = ring + s * kStageBytes + kTileBytes;
       const int valid_tokens = pc.L - j * kBlock < kBlock ? pc.L - j * kBlock : kBlock;
-      float p[4];
+      float p[NCH][4];
       if (cur_blk >= 0) {
-        float st[4];
+        float st[NCH][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) st[c] = (acc[0][c] + acc[1][c]) + (acc[2][c] + acc[3][c]);
-        // ---- online softmax of columns g0, g0+1 over tokens r4, r4+8.  Each
-        // lane checks its own scores against the running max; only when one
-        // of them exceeds it by more than 2^8 does the warp reduce the tile's
-        // column maxima and move the running max (rare after the first tile).
-        float mx[2];
+        for (int hf = 0; hf < NCH; ++hf)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if constexpr (kSc == 4)
+              st[hf][c] = (acc[hf][0][c] + acc[hf][1][c]) + (acc[hf][2][c] + acc[hf][3][c]);
+            else
+              st[hf][c] = acc[hf][0][c] + acc[hf][1][c];
+          }
+        // ---- online softmax of columns 8hf + g0, +1 over tokens r4, r4+8.
+        // Each lane checks its own scores against the running max; only when
+        // one of them exceeds it by more than 2^8 does the warp reduce the
+        // tile's column maxima and move the running max (rare after the first
+        // tile).
+        float mx[NCH][2];
         bool grow = false;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          // (rows past a column's last position; the cut can reach into the
-          // tile before the last one)
-          const int vt = kExt ? pc.L - j * kBlock - (c ? cut1 : cut0) : valid_tokens;
-          st[c] = r4 < vt ? st[c] * P.qscale : -INFINITY;
-          st[2 + c] = r4 + 8 < vt ? st[2 + c] * P.qscale : -INFINITY;
-          mx[c] = fmaxf(st[c], st[2 + c]);
-          grow = grow || mx[c] > m_run[c] + kRescaleThreshold;
-        }
-        if (__any_sync(0xffffffffu, grow)) {  // warp-uniform
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int msk = 4; msk < 32; msk <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], msk));
-          float alpha[2];
+        for (int hf = 0; hf < NCH; ++hf)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const float mn = fmaxf(m_run[c], mx[c]);
-            // (extended kernel: a column with no position seen yet stays at
-            // -inf and keeps its zero state)
-            alpha[c] = kExt && mn == -INFINITY ? 1.f : fast_exp2(m_run[c] - mn);
-            l_run[c] *= alpha[c];
-            m_run[c] = mn;
+            // (rows past a column's last position; the cut can reach into the
+            // tile before the last one)
+            const int vt = kExt ? pc.L - j * kBlock - cut[hf][c] : valid_tokens;
+            st[hf][c] = r4 < vt ? st[hf][c] * P.qscale : -INFINITY;
+            st[hf][2 + c] = r4 + 8 < vt ? st[hf][2 + c] * P.qscale : -INFINITY;
+            mx[hf][c] = fmaxf(st[hf][c], st[hf][2 + c]);
+            grow = grow || mx[hf][c] > m_run[hf][c] + kRescaleThreshold;
           }
-          if constexpr (kPvMode == 1) {
-            // columns 4-7 (low halves) belong to the heads of lane c4 - 2
-            const float x0 = __shfl_xor_sync(0xffffffffu, alpha[0], 2);
-            const float x1 = __shfl_xor_sync(0xffffffffu, alpha[1], 2);
-            const float a0 = c4 < 2 ? alpha[0] : x0, a1 = c4 < 2 ? alpha[1] : x1;
+        if (__any_sync(0xffffffffu, grow)) {  // warp-uniform
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              oc[mt][0] *= a0;
-              oc[mt][1] *= a1;
-              oc[mt][2] *= a0;
-              oc[mt][3] *= a1;
+          for (int hf = 0; hf < NCH; ++hf) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int msk = 4; msk < 32; msk <<= 1)
+                mx[hf][c] = fmaxf(mx[hf][c], __shfl_xor_sync(0xffffffffu, mx[hf][c], msk));
+            float alpha[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const float mn = fmaxf(m_run[hf][c], mx[hf][c]);
+              // (extended kernel: a column with no position seen yet stays at
+              // -inf and keeps its zero state)
+              alpha[c] = kExt && mn == -INFINITY ? 1.f : fast_exp2(m_run[hf][c] - mn);
+              l_run[hf][c] *= alpha[c];
+              m_run[hf][c] = mn;
             }
-          } else if constexpr (kPvMode == 2) {
+            if constexpr (kPvMode == 1) {
+              // columns 4-7 (low halves) belong to the heads of lane c4 - 2
+              const float x0 = __shfl_xor_sync(0xffffffffu, alpha[0], 2);
+              const float x1 = __shfl_xor_sync(0xffffffffu, alpha[1], 2);
+              const float a0 = c4 < 2 ? alpha[0] : x0, a1 = c4 < 2 ? alpha[1] : x1;
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              oc[mt][0] *= alpha[0];
-              oc[mt][1] *= alpha[1];
-              oc[mt][2] *= alpha[0];
-              oc[mt][3] *= alpha[1];
-              oc2[mt][0] *= alpha[0];
-              oc2[mt][1] *= alpha[1];
-              oc2[mt][2] *= alpha[0];
-              oc2[mt][3] *= alpha[1];
-            }
-          } else {
+              for (int mt = 0; mt < 8; ++mt) {
+                oc[hf][mt][0] *= a0;
+                oc[hf][mt][1] *= a1;
+                oc[hf][mt][2] *= a0;
+                oc[hf][mt][3] *= a1;
+              }
+            } else if constexpr (kPvMode == 2) {
 #pragma unroll
-            for (int g = 0; g < (kMmaPv ? 1 : G); ++g) {
-              const float al = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
+              for (int mt = 0; mt < 8; ++mt) {
+                oc[hf][mt][0] *= alpha[0];
+                oc[hf][mt][1] *= alpha[1];
+                oc[hf][mt][2] *= alpha[0];
+                oc[hf][mt][3] *= alpha[1];
+                if constexpr (kLoApart) {
+                  oc2[mt][0] *= alpha[0];
+                  oc2[mt][1] *= alpha[1];
+                  oc2[mt][2] *= alpha[0];
+                  oc2[mt][3] *= alpha[1];
+                }
+              }
+            } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                o[g][e].x *= al;
-                o[g][e].y *= al;
+              for (int g = 0; g < (kMmaPv ? 1 : G); ++g) {
+                const float al = __shfl_sync(0xffffffffu, alpha[g & 1], g >> 1);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  o[g][e].x *= al;
+                  o[g][e].y *= al;
+                }
               }
             }
           }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          // (extended kernel: a column may see no position of a piece yet)
-          p[k] = kExt && st[k] == -INFINITY ? 0.f : fast_exp2(st[k] - m_run[k & 1]);
-          l_run[k & 1] += p[k];
-        }
+        for (int hf = 0; hf < NCH; ++hf)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // (extended kernel: a column may see no position of a piece yet)
+            p[hf][k] = kExt && st[hf][k] == -INFINITY ? 0.f : fast_exp2(st[hf][k] - m_run[hf][k & 1]);
+            l_run[hf][k & 1] += p[hf][k];
+          }
         if constexpr (!kMmaPv) {
           if (g0 < G) {
-            pb[r4][g0] = p[0];
-            pb[r4 + 8][g0] = p[2];
+            pb[r4][g0] = p[0][0];
+            pb[r4 + 8][g0] = p[0][2];
           }
           if (g0 + 1 < G) {
-            pb[r4][g0 + 1] = p[1];
-            pb[r4 + 8][g0 + 1] = p[3];
+            pb[r4][g0 + 1] = p[0][1];
+            pb[r4 + 8][g0 + 1] = p[0][3];
           }
           __syncwarp();
         }
@@ -906,7 +998,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       // ---- next tile: wait for it and issue its score product now
       int nxt_blk = -1;
       bool nxt_touched = false;
-      float acc2[4][4];
+      float acc2[NCH][kSc][4];
       if (j + 1 < pc.j1) {
         if (!prepare(j + 1, n + 1, nxt_blk, nxt_touched))
           ok = false;
@@ -915,38 +1007,49 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       }
       if (cur_blk >= 0) {
         if constexpr (kPvMode == 2) {
-          // ---- O^T += V^T P on the tensor cores, 8 heads: the high 16-bit
-          // halves of the weights in one product, the low halves in another
-          const uint32_t bh0 = movmatrix_trans(pack_hi<kBf16>(p[0], p[1]));
-          const uint32_t bh1 = movmatrix_trans(pack_hi<kBf16>(p[2], p[3]));
-          const uint32_t bl0 = movmatrix_trans(pack_lo<kBf16>(p[0], p[1]));
-          const uint32_t bl1 = movmatrix_trans(pack_lo<kBf16>(p[2], p[3]));
+          // ---- O^T += V^T P on the tensor cores, 8 columns per half: the
+          // high 16-bit halves of the weights in one product, the low halves
+          // in another; each V fragment serves both halves
+          uint32_t bh[NCH][2], bl[NCH][2];
+#pragma unroll
+          for (int hf = 0; hf < NCH; ++hf) {
+            bh[hf][0] = movmatrix_trans(pack_hi<kBf16>(p[hf][0], p[hf][1]));
+            bh[hf][1] = movmatrix_trans(pack_hi<kBf16>(p[hf][2], p[hf][3]));
+            bl[hf][0] = movmatrix_trans(pack_lo<kBf16>(p[hf][0], p[hf][1]));
+            bl[hf][1] = movmatrix_trans(pack_lo<kBf16>(p[hf][2], p[hf][3]));
+          }
           const uint32_t vs_addr = smem_addr(Vs);
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             uint32_t a0, a1, a2, a3;
             ldsm_x4_trans(vs_addr + swz(v_tok, 2 * mt + v_cadd), a0, a1, a2, a3);
-            mma16816<kBf16>(oc[mt], a0, a1, a2, a3, bh0, bh1);
-            mma16816<kBf16>(oc2[mt], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+            for (int hf = 0; hf < NCH; ++hf) {
+              mma16816<kBf16>(oc[hf][mt], a0, a1, a2, a3, bh[hf][0], bh[hf][1]);
+              if constexpr (kLoApart)
+                mma16816<kBf16>(oc2[mt], a0, a1, a2, a3, bl[hf][0], bl[hf][1]);
+              else
+                mma16816<kBf16>(oc[hf][mt], a0, a1, a2, a3, bl[hf][0], bl[hf][1]);
+            }
           }
         } else if constexpr (kPvMode == 1) {
           // ---- O^T += V^T P on the tensor cores.  B operand: the weights as
           // a 16-token x 8-column matrix (columns 0-3: high 16-bit halves of
           // heads 0-3, columns 4-7: the low halves, so hi + lo carries p to
           // about 2^-17), transposed from the score fragment by movmatrix.
-          const float x0 = __shfl_xor_sync(0xffffffffu, p[0], 2);
-          const float x1 = __shfl_xor_sync(0xffffffffu, p[1], 2);
-          const float x2 = __shfl_xor_sync(0xffffffffu, p[2], 2);
-          const float x3 = __shfl_xor_sync(0xffffffffu, p[3], 2);
-          const uint32_t w01 = c4 < 2 ? pack_hi<kBf16>(p[0], p[1]) : pack_lo<kBf16>(x0, x1);
-          const uint32_t w23 = c4 < 2 ? pack_hi<kBf16>(p[2], p[3]) : pack_lo<kBf16>(x2, x3);
+          const float x0 = __shfl_xor_sync(0xffffffffu, p[0][0], 2);
+          const float x1 = __shfl_xor_sync(0xffffffffu, p[0][1], 2);
+          const float x2 = __shfl_xor_sync(0xffffffffu, p[0][2], 2);
+          const float x3 = __shfl_xor_sync(0xffffffffu, p[0][3], 2);
+          const uint32_t w01 = c4 < 2 ? pack_hi<kBf16>(p[0][0], p[0][1]) : pack_lo<kBf16>(x0, x1);
+          const uint32_t w23 = c4 < 2 ? pack_hi<kBf16>(p[0][2], p[0][3]) : pack_lo<kBf16>(x2, x3);
           const uint32_t b0 = movmatrix_trans(w01), b1 = movmatrix_trans(w23);
           const uint32_t vs_addr = smem_addr(Vs);
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             uint32_t a0, a1, a2, a3;
             ldsm_x4_trans(vs_addr + swz(v_tok, 2 * mt + v_cadd), a0, a1, a2, a3);
-            mma16816<kBf16>(oc[mt], a0, a1, a2, a3, b0, b1);
+            mma16816<kBf16>(oc[0][mt], a0, a1, a2, a3, b0, b1);
           }
         } else if (valid_tokens == kBlock) {  // ---- o += p V on the FMA pipes, full tile
           uint4 raw[kBlock / 2];
@@ -1003,26 +1106,31 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       cur_blk = nxt_blk;
       cur_touched = nxt_touched;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int hf = 0; hf < NCH; ++hf)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[c][e] = acc2[c][e];
+        for (int c = 0; c < kSc; ++c)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[hf][c][e] = acc2[hf][c][e];
     }
     if (!ok) break;
 
     // ---- finish the piece: per-head m and l, then the output row or a
     // partial record
-    float lsum[2];
+    float lsum[NCH][2];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      lsum[c] = l_run[c];
+    for (int hf = 0; hf < NCH; ++hf)
 #pragma unroll
-      for (int msk = 4; msk < 32; msk <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], msk);
-    }
+      for (int c = 0; c < 2; ++c) {
+        lsum[hf][c] = l_run[hf][c];
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) lsum[hf][c] += __shfl_xor_sync(0xffffffffu, lsum[hf][c], msk);
+      }
+    // column g = 8hf + gg sits in lane gg / 2 of half hf
     float mg[G], lg[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      mg[g] = __shfl_sync(0xffffffffu, m_run[g & 1], g >> 1);
-      lg[g] = __shfl_sync(0xffffffffu, lsum[g & 1], g >> 1);
+      mg[g] = __shfl_sync(0xffffffffu, m_run[g >> 3][g & 1], (g & 7) >> 1);
+      lg[g] = __shfl_sync(0xffffffffu, lsum[g >> 3][g & 1], (g & 7) >> 1);
     }
     const long long row0 = (static_cast<long long>(pc.i) * P.Hq + pc.h * G) * kHeadDim;
     float* rec = P.ws + pc.rec * record_floats(G);
@@ -1032,31 +1140,34 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
         P.lse[static_cast<long long>(pc.i) * P.Hq + pc.h * G + g] = lg[g] > 0.f ? mg[g] + __log2f(lg[g]) : -INFINITY;
     }
     if constexpr (kPvMode == 2) {
-      // o = high + low products; lane c4 holds heads 2c4, 2c4+1 at dims
-      // 16mt+r4 (entries 0, 1) and 16mt+r4+8 (entries 2, 3)
+      // o = high + low products; lane c4 holds columns 8hf + 2c4, +1 at
+      // dims 16mt+r4 (entries 0, 1) and 16mt+r4+8 (entries 2, 3)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int g = 2 * c4 + e;
-        if (g < G) {
-          float lgg = lg[0];
+      for (int hf = 0; hf < NCH; ++hf)
 #pragma unroll
-          for (int gg = 1; gg < G; ++gg)
-            if (g == gg) lgg = lg[gg];
-          const float inv = lgg > 0.f ? 1.f / lgg : 0.f;
+        for (int e = 0; e < 2; ++e) {
+          const int g = 8 * hf + 2 * c4 + e;
+          if (g < G) {
+            float lgg = lg[0];
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
+            for (int gg = 1; gg < G; ++gg)
+              if (g == gg) lgg = lg[gg];
+            const float inv = lgg > 0.f ? 1.f / lgg : 0.f;
+            const long long orow = pc.final_out ? io_at(pc.i, pc.h, g) : 0;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const float v = oc[mt][2 * hh + e] + oc2[mt][2 * hh + e];
-              const int d = 16 * mt + r4 + 8 * hh;
-              if (pc.final_out)
-                store_out(P.out, row0 + g * kHeadDim + d, v * inv, P.out_dtype);
-              else
-                rec[g * kHeadDim + d] = v;
+            for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float v = oc[hf][mt][2 * hh + e] + (kLoApart ? oc2[mt][2 * hh + e] : 0.f);
+                const int d = 16 * mt + r4 + 8 * hh;
+                if (!pc.final_out)
+                  rec[g * kHeadDim + d] = v;
+                else if (orow >= 0)
+                  store_out(P.out, orow + d, v * inv, P.out_dtype);
+              }
             }
           }
         }
-      }
     } else if constexpr (kPvMode == 1) {
       // o = high + low columns; lanes c4 and c4^2 then hold the same sums:
       // lane c4 < 2 writes dims 16mt+r4, lane c4 >= 2 dims 16mt+r4+8, of
@@ -1064,7 +1175,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) oc[mt][e] += __shfl_xor_sync(0xffffffffu, oc[mt][e], 2);
+        for (int e = 0; e < 4; ++e) oc[0][mt][e] += __shfl_xor_sync(0xffffffffu, oc[0][mt][e], 2);
       const int hsel = (c4 & 1) * 2;
       const int dadd = c4 < 2 ? 0 : 8;
 #pragma unroll
@@ -1082,7 +1193,7 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
           const float inv = lgg > 0.f ? 1.f / lgg : 0.f;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            const float v = c4 < 2 ? oc[mt][e] : oc[mt][2 + e];
+            const float v = c4 < 2 ? oc[0][mt][e] : oc[0][mt][2 + e];
             const int d = 16 * mt + r4 + dadd;
             if (pc.final_out)
               store_out(P.out, row0 + g * kHeadDim + d, v * inv, P.out_dtype);
@@ -1167,7 +1278,7 @@ template <int N>
 struct RbTag {
   static constexpr int value = N;
 };
-template <int G>
+template <int G, bool kExt>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Params P) {
   extern __shared__ int mpfx[];  // [B + 1]
   block_prefix(P, mpfx, nullptr, false);
@@ -1182,6 +1293,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     const int h = static_cast<int>(sh % P.Hkv);
     const int i = static_cast<int>(sh / P.Hkv);
     if (mpfx[i + 1] == mpfx[i]) continue;  // empty sequence: written by the decode kernel
+    const long long at = kExt && P.ext_qbase ? packed_io_offset(P, P.ext_qbase[i], P.ext_ntok[i], h, g)
+                                             : (static_cast<long long>(i) * P.Hq + h * G + g) * kHeadDim;
+    if (at < 0) continue;  // a column that carries no query
     const SegmentRecords recs(P, mpfx, i, h);
     if (recs.count <= 1) continue;  // whole segment: written by the decode kernel
     if (!waited) {  // the index math above needs only the lengths
@@ -1244,8 +1358,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         batch(RbTag<RB>{});
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    const long long idx = (static_cast<long long>(i) * P.Hq + h * G + g) * kHeadDim + 4 * lane;
-    store_out4(P.out, idx, O.x * inv, O.y * inv, O.z * inv, O.w * inv, P.out_dtype);
+    store_out4(P.out, at + 4 * lane, O.x * inv, O.y * inv, O.z * inv, O.w * inv, P.out_dtype);
     if (P.lse && lane == 0)
       P.lse[static_cast<long long>(i) * P.Hq + h * G + g] = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
   }
@@ -1259,7 +1372,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 // segment: packed sequence v holds tokens t0 .. t0 + ntok - 1 of sequence i,
 // its length is the last token's position + 1, column tt*G + g is token
 // t0 + tt's query head g, and token t0 + tt sees ntok - 1 - tt positions
-// fewer.  Every K/V tile of the prefix is read once per TC tokens.
+// fewer.  Every K/V tile of the prefix is read once per TC tokens.  The plan
+// kernel writes the packed lengths and each packed sequence's first query
+// row (its column blocks carry that row and the ones after it); the decode
+// and merge kernels read q and write out at those rows, so nothing is copied
+// into or out of a packed layout.
 // ---------------------------------------------------------------------------
 struct MultiPlan {
   const int32_t* q_start;   // [B + 1]
@@ -1268,8 +1385,7 @@ struct MultiPlan {
   int32_t* lens_v;          // [Bv]
   int32_t* offs_v;          // [Bv]
   int32_t* ntok_v;          // [Bv]
-  int32_t* qrow;            // [Bv * TC]: query row of column block tt, or -1
-  int32_t* rowmap;          // [n_q]: v * TC + tt of query row r
+  int32_t* qbase_v;         // [Bv]: query row of column block 0, or -1 (no query rows)
   long long* err;
 };
 
@@ -1280,6 +1396,9 @@ __global__ void __launch_bounds__(1024) multi_plan_kernel(MultiPlan M) {
   __shared__ int carry_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int cap = M.max_blocks * kBlock;
+  // the decode that reads the plan is launched as this grid's dependent and
+  // waits for it to complete before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) carry_s = 0;
   __syncthreads();
   for (int base = 0; base < M.B; base += blockDim.x) {
@@ -1318,12 +1437,11 @@ __global__ void __launch_bounds__(1024) multi_plan_kernel(MultiPlan M) {
         M.lens_v[v] = bad ? 0 : L - T + t0 + nt;
         M.offs_v[v] = i * M.max_blocks;
         M.ntok_v[v] = nt;
-        for (int tt = 0; tt < M.TC; ++tt) {
-          const int r = M.q_start[i] + t0 + tt;
-          const bool real = tt < nt && r >= 0 && r < M.n_q;
-          M.qrow[v * M.TC + tt] = real ? r : -1;
-          if (real) M.rowmap[r] = v * M.TC + tt;
-        }
+        // column block tt carries row r0 + tt (tt < nt)
+        const int r0 = M.q_start[i] + t0;
+        const bool rows_ok = r0 >= 0 && r0 + nt <= M.n_q;
+        if (!rows_ok) record_error(M.err, PA_ERR_DEVICE_CHECK, i);
+        M.qbase_v[v] = rows_ok ? r0 : -1;
       }
     }
     __syncthreads();
@@ -1334,42 +1452,8 @@ __global__ void __launch_bounds__(1024) multi_plan_kernel(MultiPlan M) {
     M.lens_v[v] = 0;
     M.offs_v[v] = 0;
     M.ntok_v[v] = 1;
-    for (int tt = 0; tt < M.TC; ++tt) M.qrow[v * M.TC + tt] = -1;
+    M.qbase_v[v] = -1;
   }
-}
-
-// q of the packed sequences: row (v*Hkv + h)*GP + tt*G + g, zero for unused
-// column blocks.  One thread per 16-byte vector.
-__global__ void multi_pack_kernel(const uint4* __restrict__ q, const int32_t* __restrict__ qrow, int Bv, int Hkv,
-                                  int G, int TC, int Hq, uint4* __restrict__ qv) {
-  const int GP = G * TC;
-  const long long n_vec = static_cast<long long>(Bv) * Hkv * GP * (kHeadDim / 8);
-  for (long long x = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; x < n_vec;
-       x += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = x / (kHeadDim / 8);
-    const int w = static_cast<int>(x % (kHeadDim / 8));
-    const int col = static_cast<int>(row % GP);
-    const long long vh = row / GP;
-    const int h = static_cast<int>(vh % Hkv);
-    const long long v = vh / Hkv;
-    const int r = qrow[v * TC + col / G];
-    qv[x] = r >= 0 ? q[((static_cast<long long>(r) * Hq + h * G + col % G) * kHeadDim) / 8 + w]
-                   : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// One warp per (query row, query head): out[r][hq] from the packed output.
-__global__ void multi_unpack_kernel(const float* __restrict__ ov, const int32_t* __restrict__ rowmap, int n_q,
-                                    int Hkv, int G, int TC, void* out, int out_dtype) {
-  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int Hq = Hkv * G, GP = G * TC;
-  if (wid >= static_cast<long long>(n_q) * Hq) return;
-  const int r = static_cast<int>(wid / Hq), hq = static_cast<int>(wid % Hq);
-  const int vt = rowmap[r];
-  const long long src = (static_cast<long long>(vt / TC) * Hkv + hq / G) * GP + (vt % TC) * G + hq % G;
-  const float4 o = reinterpret_cast<const float4*>(ov + src * kHeadDim)[lane];
-  store_out4(out, wid * kHeadDim + 4 * lane, o.x, o.y, o.z, o.w, out_dtype);
 }
 
 // ---------------------------------------------------------------------------
@@ -1584,7 +1668,7 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
   }
   if (grid < 1) grid = 1;
   P.lean_units = static_cast<int>(grid) * NW;
-  const bool secondary = kExt && (P.launch_flags & kLaunchSecondary);
+  const bool secondary = kExt && (P.launch_flags & (kLaunchSecondary | kLaunchAfterPlan));
   const bool with_decode = !(P.launch_flags & kLaunchMergeOnly);
   const bool with_merge = P.sched != SCHED_SEGMENT && !(P.launch_flags & kLaunchNoMerge);
   if (kFused && !with_decode) return PA_ERR_INVALID;
@@ -1631,7 +1715,7 @@ static int launch_typed(Params& P, int device, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, merge_kernel<G>, P) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, merge_kernel<G, kExt>, P) != cudaSuccess) return PA_ERR_CUDA;
   }
   if (timed) {
     if (cudaEventRecord(g_prof_events[2 * g_prof_next + 1], stream) != cudaSuccess) return PA_ERR_CUDA;
@@ -1651,6 +1735,9 @@ static int launch_g(int G, Params& P, int device, cudaStream_t stream) {
     case 6: return launch_typed<6, kBf16, kFused, kExt>(P, device, stream);
     case 7: return launch_typed<7, kBf16, kFused, kExt>(P, device, stream);
     case 8: return launch_typed<8, kBf16, kFused, kExt>(P, device, stream);
+    case kMaxPackedCols:  // packed tokens only (two column halves)
+      if constexpr (kExt && !kFused) return launch_typed<kMaxPackedCols, kBf16, kFused, kExt>(P, device, stream);
+      return PA_ERR_UNSUPPORTED;
     default: return PA_ERR_UNSUPPORTED;
   }
 }
@@ -1661,11 +1748,11 @@ struct WorkspaceLayout {
 };
 
 static bool workspace_layout(const pa_pool* p, int B, int Hq, int max_blocks, int partition_blocks,
-                             WorkspaceLayout* out) {
+                             WorkspaceLayout* out, int max_g = PA_MAX_GROUP) {
   if (!p || B <= 0 || Hq <= 0 || max_blocks <= 0 || partition_blocks < 0) return false;
   if (Hq % p->n_kv_heads) return false;
   int G = Hq / p->n_kv_heads;
-  if (G > PA_MAX_GROUP) return false;
+  if (G > max_g) return false;
   size_t rec = sizeof(float) * record_floats(G);
   size_t n_rec;
   if (partition_blocks == 0)  // LEAN: two records per warp of the largest grid
@@ -1683,23 +1770,33 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
                          int Hq, float scale, void* out, int out_dtype, int sched,
                          int partition_blocks, void* ws, size_t ws_bytes, void* stream,
                          const int32_t* table_offs = nullptr, float* lse = nullptr,
-                         const int32_t* ext_ntok = nullptr, int ext_g = 0, int launch_flags = 0) {
+                         const int32_t* ext_ntok = nullptr, int ext_g = 0, int launch_flags = 0,
+                         const int32_t* ext_qbase = nullptr, int ext_hq = 0) {
   if (!p || !q || !tables || !seq_lens || !out || B <= 0 || Hq <= 0 || max_blocks <= 0)
     return PA_ERR_INVALID;
   if (out_dtype != PA_FP16 && out_dtype != PA_BF16 && out_dtype != PA_FP32) return PA_ERR_INVALID;
   if (Hq % p->n_kv_heads) return PA_ERR_INVALID;
   const int G = Hq / p->n_kv_heads;
-  if (G > PA_MAX_GROUP) return PA_ERR_UNSUPPORTED;
+  // (more than 8 columns: packed query tokens only)
+  const int max_g = ext_qbase ? kMaxPackedCols : PA_MAX_GROUP;
+  if (G > max_g) return PA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PA_ERR_INVALID;
   const bool fused = k_new != nullptr;
   if (fused && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15))
     return PA_ERR_INVALID;
   if ((table_offs || lse) && (sched == SCHED_SEGMENT || fused)) return PA_ERR_INVALID;
+  // packed tokens in q / out rows: ext_g columns each in the G, columns past the
+  // last whole token empty (no log2-sum-exp out)
+  if (ext_qbase && (!table_offs || !ext_ntok || lse || ext_g <= 0 || ext_g > G || ext_hq <= 0 ||
+                    ext_hq % p->n_kv_heads || ext_hq / p->n_kv_heads != ext_g))
+    return PA_ERR_INVALID;
+  // (only the 8-column value path of groups above 4 writes packed rows)
+  if (ext_qbase && G <= 4) return PA_ERR_UNSUPPORTED;
   if (!on_pool_device(p)) return PA_ERR_INVALID;  // the kernels run on the current device
   WorkspaceLayout lay{};
   if (sched != SCHED_SEGMENT) {
     if (B > kMaxSplitSeqs) return PA_ERR_UNSUPPORTED;
-    if (!workspace_layout(p, B, Hq, max_blocks, partition_blocks, &lay)) return PA_ERR_INVALID;
+    if (!workspace_layout(p, B, Hq, max_blocks, partition_blocks, &lay, max_g)) return PA_ERR_INVALID;
     if (!ws || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(ws) & 15)) return PA_ERR_INVALID;
   }
   Params P{};
@@ -1714,6 +1811,8 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.lse = lse;
   P.ext_ntok = ext_ntok;
   P.ext_g = ext_g > 0 ? ext_g : 1;
+  P.ext_qbase = ext_qbase;
+  P.ext_hq = ext_hq;
   P.seq_lens = seq_lens;
   P.out = out;
   P.ws = static_cast<float*>(ws);
@@ -1819,8 +1918,8 @@ int pa_append_decode(pa_pool_t p, const void* q, const void* k_new, const void* 
 
 // Multi-token queries: workspace pieces, each 256-byte aligned.
 struct MultiLayout {
-  int TC, Bv;
-  size_t lens_v, offs_v, ntok_v, qrow, rowmap, qv, ov, rec, total;
+  int TC, GP, Bv;  // tokens per packed sequence, kernel columns, packed sequences
+  size_t lens_v, offs_v, ntok_v, qbase_v, rec, total;
 };
 static bool multi_layout(const pa_pool* p, int n_q, int B, int Hq, int max_blocks, MultiLayout* L) {
   if (!p || n_q <= 0 || B <= 0 || Hq <= 0 || max_blocks <= 0 || Hq % p->n_kv_heads) return false;
@@ -1828,25 +1927,25 @@ static bool multi_layout(const pa_pool* p, int n_q, int B, int Hq, int max_block
   if (static_cast<long long>(B) * max_blocks > 0x7fffffffll) return false;
   const int G = Hq / p->n_kv_heads;
   if (G > PA_MAX_GROUP) return false;
-  L->TC = PA_MAX_GROUP / G;
+  // Sixteen columns (two halves sharing each tile) when the sequences carry
+  // more than 8 columns of new tokens on average, else the 8 of one MMA
+  // (whole tokens in both cases; columns past the last token stay empty).
+  const bool wide = static_cast<long long>(n_q) * G > 8ll * B;
+  L->TC = (wide ? kMaxPackedCols : PA_MAX_GROUP) / G;
+  L->GP = wide ? kMaxPackedCols : G * L->TC;
   L->Bv = (n_q + L->TC - 1) / L->TC + B;  // every sequence's last pack may be partial
-  const int GP = G * L->TC;
   WorkspaceLayout rw{};
-  if (!workspace_layout(p, L->Bv, p->n_kv_heads * GP, max_blocks, 0, &rw)) return false;
+  if (!workspace_layout(p, L->Bv, p->n_kv_heads * L->GP, max_blocks, 0, &rw, kMaxPackedCols)) return false;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
     off += (bytes + 255) / 256 * 256;
     return at;
   };
-  const size_t rows_v = static_cast<size_t>(L->Bv) * p->n_kv_heads * GP;
   L->lens_v = take(sizeof(int32_t) * L->Bv);
   L->offs_v = take(sizeof(int32_t) * L->Bv);
   L->ntok_v = take(sizeof(int32_t) * L->Bv);
-  L->qrow = take(sizeof(int32_t) * static_cast<size_t>(L->Bv) * L->TC);
-  L->rowmap = take(sizeof(int32_t) * static_cast<size_t>(n_q));
-  L->qv = take(rows_v * kHeadDim * 2);
-  L->ov = take(rows_v * kHeadDim * 4);
+  L->qbase_v = take(sizeof(int32_t) * L->Bv);
   L->rec = take(rw.total);
   L->total = off;
   return true;
@@ -1873,7 +1972,7 @@ int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return PA_ERR_INVALID;
   char* ws = static_cast<char*>(workspace);
-  const int Hkv = p->n_kv_heads, G = n_q_heads / Hkv, GP = G * L.TC;
+  const int Hkv = p->n_kv_heads, G = n_q_heads / Hkv, GP = L.GP;
   MultiPlan M{};
   M.q_start = q_start;
   M.seq_lens = seq_lens;
@@ -1885,27 +1984,15 @@ int pa_decode_multi(pa_pool_t p, const void* q, const int32_t* q_start, int n_q,
   M.lens_v = reinterpret_cast<int32_t*>(ws + L.lens_v);
   M.offs_v = reinterpret_cast<int32_t*>(ws + L.offs_v);
   M.ntok_v = reinterpret_cast<int32_t*>(ws + L.ntok_v);
-  M.qrow = reinterpret_cast<int32_t*>(ws + L.qrow);
-  M.rowmap = reinterpret_cast<int32_t*>(ws + L.rowmap);
+  M.qbase_v = reinterpret_cast<int32_t*>(ws + L.qbase_v);
   M.err = p->err;
   cudaStream_t st = as_stream(stream);
-  // rows the plan never maps (a broken q_start) read packed row 0 of sequence 0
-  if (cudaMemsetAsync(M.rowmap, 0, sizeof(int32_t) * static_cast<size_t>(n_q), st) != cudaSuccess) return PA_ERR_CUDA;
   multi_plan_kernel<<<1, 1024, 0, st>>>(M);
-  const long long n_vec = static_cast<long long>(L.Bv) * Hkv * GP * (kHeadDim / 8);
-  const int pack_grid = static_cast<int>(n_vec < 4096 * 256 ? (n_vec + 255) / 256 : 4096);
-  multi_pack_kernel<<<pack_grid, 256, 0, st>>>(static_cast<const uint4*>(q), M.qrow, L.Bv, Hkv, G, L.TC, n_q_heads,
-                                               reinterpret_cast<uint4*>(ws + L.qv));
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  float* ov = reinterpret_cast<float*>(ws + L.ov);
-  const int rc = decode_common(p, ws + L.qv, nullptr, nullptr, block_tables, max_blocks_per_seq, M.lens_v, L.Bv,
-                               Hkv * GP, scale, ov, PA_FP32, SCHED_LEAN, 0, ws + L.rec, L.total - L.rec, stream,
-                               M.offs_v, nullptr, M.ntok_v, G);
-  if (rc != PA_OK) return rc;
-  const long long warps = static_cast<long long>(n_q) * n_q_heads;
-  multi_unpack_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(ov, M.rowmap, n_q, Hkv, G, L.TC,
-                                                                                     out, out_dtype);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  // the decode and its merge read q and write out at the plan's rows
+  return decode_common(p, q, nullptr, nullptr, block_tables, max_blocks_per_seq, M.lens_v, L.Bv, Hkv * GP, scale,
+                       out, out_dtype, SCHED_LEAN, 0, ws + L.rec, L.total - L.rec, stream, M.offs_v, nullptr,
+                       M.ntok_v, G, kLaunchAfterPlan, M.qbase_v, n_q_heads);
 }
 
 // Shared-prefix decode: workspace pieces, each 256-byte aligned.

@@ -82,6 +82,14 @@ class GpuCase:
     def appended_pools(self):
         return oracle.cache.append(self.kp, self.vp, self.kn, self.vn, self.slots)
 
+    def vmax(self):
+        """max |v| over the V values the step attends (pool after the append;
+        the NaN sentinels of unused slots excluded)."""
+        _, vp = self.appended_pools()
+        v = torch.from_numpy(np.ascontiguousarray(vp).view(np.int16)).view(self.dtype).float().abs()
+        v = v[torch.isfinite(v)]
+        return float(v.max()) if v.numel() else 0.0
+
     def reference(self, after_append=True, rows=None):
         if after_append:
             kp, vp = self.appended_pools()
@@ -102,23 +110,27 @@ def assert_close(out, ref, what=""):
     return err
 
 
-# Absolute error floor of the native 16-bit check: the fp32 arithmetic
-# (2e-6), plus the value product's weights, which the tensor-core path (G <= 4)
-# carries as a high and a low 16-bit half, i.e. to 2^-18 relative; summed over
-# values |v| <= 6 (N(0,1) samples) that is at most 2^-18 * 6 per output.
-FP32_FLOOR = 2e-6 + 2.0 ** -18 * 6.0
+def fp32_floor(vmax):
+    """Absolute error floor of the native 16-bit check: the fp32 arithmetic
+    (2e-6), plus the value product's weights, which the tensor-core path
+    carries as a high and a low 16-bit half, i.e. to 2^-18 relative: summed
+    with weights that add up to 1 over values |v| <= vmax, that is at most
+    2^-18 * vmax per output."""
+    return 2e-6 + 2.0 ** -18 * float(vmax)
 
 
-def assert_within_one_ulp16(out16, ref, dtype, what=""):
-    """Native 16-bit output: |out - RN16(ref)| <= 1 ulp of RN16(ref) + FP32_FLOOR.
+def assert_within_one_ulp16(out16, ref, dtype, what="", vmax=None):
+    """Native 16-bit output: |out - RN16(ref)| <= 1 ulp of RN16(ref) + fp32_floor(vmax).
     The absolute term covers outputs so small that one 16-bit ulp (down to
     2^-24 for fp16) is below the kernel's own error (fp32 accumulation and
-    17-bit weights on the tensor-core value path)."""
+    17-bit weights on the tensor-core value path).  vmax: max |v| of the
+    attended values (required)."""
+    assert vmax is not None, "pass the case's max |v| (GpuCase.vmax())"
     r16 = torch.from_numpy(ref).to(torch.float32).to(dtype).to(torch.float64).numpy()
     got = out16.detach().cpu().to(torch.float64).numpy().reshape(ref.shape)
     mant = 7 if dtype == torch.bfloat16 else 10
     min_exp = -126 if dtype == torch.bfloat16 else -14
     e = np.floor(np.log2(np.maximum(np.abs(r16), 2.0 ** min_exp)))
     ulp = 2.0 ** (e - mant)
-    bad = np.abs(got - r16) > ulp + FP32_FLOOR
+    bad = np.abs(got - r16) > ulp + fp32_floor(vmax)
     assert not bad.any(), f"{what}: {bad.sum()} elements more than 1 ulp from RN16(ref)"

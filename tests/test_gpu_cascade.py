@@ -80,7 +80,8 @@ def test_native_16bit_output(pa):
     c = GpuCase(4, lens=[2100, 2500, 2048, 3000, 2200, 2600])
     out, code, _ = cascade(pa, c, c.tables, c.dec_lens, out_dtype=torch.float16)
     assert code == 0
-    assert_within_one_ulp16(out.cpu(), reference(c, c.tables, c.dec_lens), torch.float16, "cascade fp16 out")
+    assert_within_one_ulp16(out.cpu(), reference(c, c.tables, c.dec_lens), torch.float16, "cascade fp16 out",
+                            vmax=c.vmax())
 
 
 def test_a_group_that_shares_nothing_is_reported_and_ignored(pa):
