@@ -121,9 +121,21 @@ struct Params {
 // its lengths, table offsets and row maps, and waits for it before reading them.
 constexpr int kLaunchSecondary = 1, kLaunchNoMerge = 2, kLaunchMergeOnly = 4, kLaunchAfterPlan = 8;
 
-// Partial record of one piece: o[G][128], then m[g] at G*128+g and l[g] at
-// G*128+64+g (fp32; m in log2 units of the scaled scores).
-__host__ __device__ constexpr int record_floats(int G) { return (G + 1) * 128; }
+// Partial record of one piece: the unnormalised output o of its columns in
+// C = record_cols(G) columns' room, then m[g] at C*128+g and l[g] at
+// C*128+64+g (fp32; m in log2 units of the scaled scores).  o is stored
+// o[g][128] by the FMA and 4-column tensor-core paths, and in fragment order
+// by the 8-column tensor-core path of the extended kernel (see
+// frag_record_index), which writes it with whole-warp 16-byte stores.
+__host__ __device__ constexpr int record_cols(int G) { return G <= 4 ? G : (G + 7) / 8 * 8; }
+__host__ __device__ constexpr int record_floats(int G) { return (record_cols(G) + 1) * 128; }
+// Fragment order: float4 number ((hf*2 + e)*4 + k)*32 + lane holds, for the
+// lane's column 8hf + 2(lane%4) + e, dims 32k + lane/4 + {0, 8, 16, 24}.
+// Returns that float4's index for column g, and the merge lane ml = 8k + r
+// whose dims are 32k + r + {0, 8, 16, 24}.
+__host__ __device__ constexpr int frag_record_index(int g, int ml) {
+  return (((g >> 3) * 2 + (g & 1)) * 4 + (ml >> 3)) * 32 + 4 * (ml & 7) + ((g & 7) >> 1);
+}
 // Columns of one segment of packed query tokens (two halves of the MMA's 8).
 constexpr int kMaxPackedCols = 16;
 
@@ -614,14 +626,17 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
   if (P.sched != SCHED_SEGMENT) {
     for (int i = blockIdx.x; i < P.B; i += gridDim.x) {
       if (S.pfx[i + 1] != S.pfx[i]) continue;
-      for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x) {
-        if constexpr (kExt) {
-          const int col = x / kHeadDim;
+      if constexpr (kExt) {
+        if (P.ext_qbase && S_rows[2 * P.B + i] < 0) continue;  // a packed slot with no query rows
+        // one warp per column; columns that carry no query are skipped
+        for (int col = warp; col < P.Hq; col += NW) {
           const long long at = io_at(i, col / G, col % G);
-          if (at >= 0) store_out(P.out, at + x % kHeadDim, 0.f, P.out_dtype);
-        } else {
-          store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
+          if (at < 0) continue;
+          for (int d = lane; d < kHeadDim; d += 32) store_out(P.out, at + d, 0.f, P.out_dtype);
         }
+      } else {
+        for (int x = threadIdx.x; x < P.Hq * kHeadDim; x += blockDim.x)
+          store_out(P.out, static_cast<long long>(i) * P.Hq * kHeadDim + x, 0.f, P.out_dtype);
       }
       if (kExt && P.lse)
         for (int x = threadIdx.x; x < P.Hq; x += blockDim.x) P.lse[static_cast<long long>(i) * P.Hq + x] = -INFINITY;
@@ -1142,29 +1157,40 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
     if constexpr (kPvMode == 2) {
       // o = high + low products; lane c4 holds columns 8hf + 2c4, +1 at
       // dims 16mt+r4 (entries 0, 1) and 16mt+r4+8 (entries 2, 3)
+      auto ov = [&](int hf, int mt, int j) {
+        return oc[hf][mt][j] + (kLoApart ? oc2[mt][j] : 0.f);
+      };
+      if (!pc.final_out) {
+        // a partial record in fragment order: per (hf, e, k) one 16-byte
+        // store per lane, 512 contiguous bytes per warp
+        float4* rec4 = reinterpret_cast<float4*>(rec);
+#pragma unroll
+        for (int hf = 0; hf < NCH; ++hf)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              rec4[((hf * 2 + e) * 4 + k) * 32 + lane] =
+                  make_float4(ov(hf, 2 * k, e), ov(hf, 2 * k, 2 + e), ov(hf, 2 * k + 1, e), ov(hf, 2 * k + 1, 2 + e));
+      }
 #pragma unroll
       for (int hf = 0; hf < NCH; ++hf)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int g = 8 * hf + 2 * c4 + e;
-          if (g < G) {
+          if (pc.final_out && g < G) {
             float lgg = lg[0];
 #pragma unroll
             for (int gg = 1; gg < G; ++gg)
               if (g == gg) lgg = lg[gg];
             const float inv = lgg > 0.f ? 1.f / lgg : 0.f;
-            const long long orow = pc.final_out ? io_at(pc.i, pc.h, g) : 0;
+            const long long orow = io_at(pc.i, pc.h, g);
+            if (orow >= 0) {
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
+              for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const float v = oc[hf][mt][2 * hh + e] + (kLoApart ? oc2[mt][2 * hh + e] : 0.f);
-                const int d = 16 * mt + r4 + 8 * hh;
-                if (!pc.final_out)
-                  rec[g * kHeadDim + d] = v;
-                else if (orow >= 0)
-                  store_out(P.out, orow + d, v * inv, P.out_dtype);
-              }
+                for (int hh = 0; hh < 2; ++hh)
+                  store_out(P.out, orow + 16 * mt + r4 + 8 * hh, ov(hf, mt, 2 * hh + e) * inv, P.out_dtype);
             }
           }
         }
@@ -1232,11 +1258,23 @@ __global__ void __launch_bounds__(Shape<G>::kThreads, Shape<G>::kMinCtas) decode
       }
     }
     if (!pc.final_out) {
-      if (lane == 0) {
+      if constexpr (kPvMode == 2) {  // lane g writes column g's m and l
+        float mv = mg[0], lv = lg[0];
+#pragma unroll
+        for (int gg = 1; gg < G; ++gg)
+          if (lane == gg) {
+            mv = mg[gg];
+            lv = lg[gg];
+          }
+        if (lane < G) {
+          rec[record_cols(G) * kHeadDim + lane] = mv;
+          rec[record_cols(G) * kHeadDim + 64 + lane] = lv;
+        }
+      } else if (lane == 0) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          rec[G * kHeadDim + g] = mg[g];
-          rec[G * kHeadDim + 64 + g] = lg[g];
+          rec[record_cols(G) * kHeadDim + g] = mg[g];
+          rec[record_cols(G) * kHeadDim + 64 + g] = lg[g];
         }
       }
     }
@@ -1285,6 +1323,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const int lane = threadIdx.x & 31;
   const long long wpb = kMergeThreads / 32;
   const long long n_items = static_cast<long long>(P.B) * P.Hkv * G;
+  // records of the extended kernel's 8-column tensor-core path are in fragment order
+  constexpr bool kFrag = kExt && G > 4;
   constexpr int RB = 16;  // records whose o loads are in flight together (4 for short lists)
   bool waited = false;
   for (long long it = blockIdx.x * wpb + (threadIdx.x >> 5); it < n_items; it += gridDim.x * wpb) {
@@ -1308,8 +1348,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       const int cnt = recs.count - c0 < 32 ? recs.count - c0 : 32;
       const bool have = lane < cnt;
       const float* rl = P.ws + recs.at(P, c0 + (have ? lane : 0)) * record_floats(G);
-      const float mv = __ldcg(rl + G * kHeadDim + g);
-      const float lv = __ldcg(rl + G * kHeadDim + 64 + g);
+      const float mv = __ldcg(rl + record_cols(G) * kHeadDim + g);
+      const float lv = __ldcg(rl + record_cols(G) * kHeadDim + 64 + g);
       const float mk = have ? mv : -INFINITY;
       const float lk = have ? lv : 0.f;
       float wk = 0.f;
@@ -1320,8 +1360,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 #pragma unroll
           for (int r = 0; r < RBv; ++r) {
             const int k = b0 + r < cnt ? b0 + r : 0;
-            ob[r] = __ldcg(reinterpret_cast<const float4*>(P.ws + recs.at(P, c0 + k) * record_floats(G) +
-                                                           g * kHeadDim) + lane);
+            const float4* r4p = reinterpret_cast<const float4*>(P.ws + recs.at(P, c0 + k) * record_floats(G));
+            ob[r] = __ldcg(r4p + (kFrag ? frag_record_index(g, lane) : g * (kHeadDim / 4) + lane));
           }
           if (b0 == 0) {  // this chunk's weights; rescale what came before
             float mx = mk;
@@ -1358,7 +1398,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         batch(RbTag<RB>{});
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    store_out4(P.out, at + 4 * lane, O.x * inv, O.y * inv, O.z * inv, O.w * inv, P.out_dtype);
+    if constexpr (kFrag) {  // this lane's dims are 32k + r + {0, 8, 16, 24}
+      const long long d0 = at + 32 * (lane >> 3) + (lane & 7);
+      store_out(P.out, d0, O.x * inv, P.out_dtype);
+      store_out(P.out, d0 + 8, O.y * inv, P.out_dtype);
+      store_out(P.out, d0 + 16, O.z * inv, P.out_dtype);
+      store_out(P.out, d0 + 24, O.w * inv, P.out_dtype);
+    } else {
+      store_out4(P.out, at + 4 * lane, O.x * inv, O.y * inv, O.z * inv, O.w * inv, P.out_dtype);
+    }
     if (P.lse && lane == 0)
       P.lse[static_cast<long long>(i) * P.Hq + h * G + g] = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
   }
