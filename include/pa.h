@@ -211,8 +211,9 @@ int pa_append_decode(pa_pool_t pool, const void* q, const void* k_new,
  * ceil(n_q / (8/G)) + num_seqs <= 4096 (else PA_ERR_UNSUPPORTED);
  * num_seqs * max_blocks_per_seq < 2^31 (else PA_ERR_INVALID).  A
  * sequence with T_i > L_i, or a length out of range, records
- * PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros; rows that a q_start
- * breaking its rules leaves to no sequence are not written. */
+ * PA_ERR_DEVICE_CHECK (pa_check) and outputs zeros.  A q_start that
+ * decreases or does not run from 0 to n_q records PA_ERR_DEVICE_CHECK; rows
+ * it leaves to no sequence are not written. */
 size_t pa_decode_multi_workspace_bytes(pa_pool_t pool, int n_q, int num_seqs,
                                        int n_q_heads, int max_blocks_per_seq);
 int pa_decode_multi(pa_pool_t pool, const void* q, const int32_t* q_start, int n_q,

@@ -1456,6 +1456,9 @@ __global__ void __launch_bounds__(1024) multi_plan_kernel(MultiPlan M) {
       T = M.q_start[i + 1] - M.q_start[i];
       L = M.seq_lens[i];
       V = T > 0 ? (T + M.TC - 1) / M.TC : 0;
+      // q_start must not decrease and must run from 0 to n_q
+      if (T < 0 || (i == 0 && M.q_start[0] != 0) || (i == M.B - 1 && M.q_start[M.B] != M.n_q))
+        record_error(M.err, PA_ERR_DEVICE_CHECK, i);
     }
     int incl = V;
 #pragma unroll

@@ -109,3 +109,24 @@ def test_more_new_tokens_than_the_sequence_is_reported(pa):
     assert code == pa.PA_ERR_DEVICE_CHECK
     assert (out[3:7] == 0).all(), "rows that would sit before position 0 output zeros"
     assert torch.isfinite(out[7:]).all() and not (out[7:] == 7.0).any()
+
+
+@pytest.mark.parametrize("q_start", [
+    [0, 3, 2, 6],                 # decreases
+    [1, 3, 4, 6],                 # does not start at 0
+    [0, 2, 4, 5],                 # ends before n_q = 6
+])
+def test_malformed_q_start_is_reported(pa, q_start):
+    """Only rows inside [0, n_q) are ever touched; the plan reports the
+    malformed offsets through pa_check."""
+    c = GpuCase(3, lens=[10, 20, 30])
+    pool = c.pool()
+    n_q = 6
+    q = torch.randn(n_q, c.cfg.n_q_heads, 128).to(c.dtype).cuda()
+    out = torch.zeros((n_q, c.cfg.n_q_heads, 128), device="cuda")
+    qs = torch.tensor(q_start, dtype=torch.int32, device="cuda")
+    pa.pa_decode_multi(pool, q, qs, c.tables_dev(), c.lens_dev(), c.case.scale, out)
+    torch.cuda.synchronize()
+    code, _ = pa.pa_check(pool)
+    assert code == pa.PA_ERR_DEVICE_CHECK
+    assert torch.isfinite(out).all()
