@@ -63,6 +63,11 @@ constexpr int kLeanMinBlocks = 4;    // smallest LEAN range per warp
 // starting a piece (its q, table window and record) in tile-equivalents, so
 // a warp whose range crosses several short segments gets fewer tiles.
 constexpr int kLeanPieceCost = 1;
+// The same for segments of packed query tokens (16 columns): a piece there
+// also costs its 8.7 KB record and a merge of 16 columns; swept 1-20 on the
+// batch-64 LLaMA-3-8B layout with 4 new tokens per sequence, 8-20 flat, 12
+// best (60.3 us against 71.2 us at 1).
+constexpr int kLeanPieceCostPacked = 12;
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -1878,7 +1883,9 @@ static int decode_common(pa_pool_t p, const void* q, const void* k_new, const vo
   P.sched = sched;
   P.partition_blocks = partition_blocks > 0 ? partition_blocks : 1;
   P.lean_units = 1;
-  P.lean_cost = kLeanPieceCost;
+  // (8-column packing keeps the plain cost: one token per sequence then splits
+  // exactly like the plain decode, bit for bit)
+  P.lean_cost = ext_qbase && G > 8 ? kLeanPieceCostPacked : kLeanPieceCost;
   P.wait_limit_ns = wait_limit_ns();
   P.launch_flags = launch_flags;
   cudaStream_t st = as_stream(stream);
