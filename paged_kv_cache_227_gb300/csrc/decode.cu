@@ -1321,8 +1321,10 @@ template <int N>
 struct RbTag {
   static constexpr int value = N;
 };
+// (16-column packed segments: short record lists and 3-4x the items, so
+// batches of 4 and 64 registers, 8 CTAs per SM: every item in one wave)
 template <int G, bool kExt>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kMergeThreads, (kExt && G > 8) ? 8 : 4) merge_kernel(const __grid_constant__ Params P) {
   extern __shared__ int mpfx[];  // [B + 1]
   block_prefix(P, mpfx, nullptr, false);
   const int lane = threadIdx.x & 31;
@@ -1330,7 +1332,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const long long n_items = static_cast<long long>(P.B) * P.Hkv * G;
   // records of the extended kernel's 8-column tensor-core path are in fragment order
   constexpr bool kFrag = kExt && G > 4;
-  constexpr int RB = 16;  // records whose o loads are in flight together (4 for short lists)
+  constexpr int RB = kExt && G > 8 ? 4 : 16;  // records whose o loads are in flight together (4 for short lists)
   bool waited = false;
   for (long long it = blockIdx.x * wpb + (threadIdx.x >> 5); it < n_items; it += gridDim.x * wpb) {
     const int g = static_cast<int>(it % G);
