@@ -1423,8 +1423,10 @@ __global__ void __launch_bounds__(kMergeThreads, (kExt && G > 8) ? 8 : 4) merge_
 // ---------------------------------------------------------------------------
 // Several new query tokens per sequence.  Sequence i's T_i new tokens are its
 // last T_i positions; token t sees positions 0 .. L_i - T_i + t.  They are
-// packed TC at a time (TC = 8 / G) into the columns of one extended-kernel
-// segment: packed sequence v holds tokens t0 .. t0 + ntok - 1 of sequence i,
+// packed TC at a time (TC = 8 / G, or 16 / G in two column halves when the
+// sequences average more than 8 columns of new tokens) into the columns of
+// one extended-kernel segment: packed sequence v holds tokens t0 .. t0 +
+// ntok - 1 of sequence i,
 // its length is the last token's position + 1, column tt*G + g is token
 // t0 + tt's query head g, and token t0 + tt sees ntok - 1 - tt positions
 // fewer.  Every K/V tile of the prefix is read once per TC tokens.  The plan
